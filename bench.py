@@ -1,0 +1,421 @@
+"""Benchmark of one paged-decode step on GB300.
+
+A step is the whole hot path over one batch: pa_reshape_and_cache (write each
+sequence's newest K/V through its slot) then pa_decode (paged attention, with
+split-context partitions joined by log-sum-exp when the workload uses them).
+
+Default workload: the Llama-3-8B-shaped GQA decode batch (64 sequences, 32
+query / 8 KV heads, head_dim 128, block_size 16, context lengths U[512,4096],
+fp16, 512-token partitions).  Inputs are seeded synthetic data resident in HBM;
+the KV bytes read per step (~0.6 GB) exceed the 129 MB L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0).  `value` is KV GB/s: algorithmic bytes per step
+(K and V of exactly the context tokens, q in and out, the block-table entries
+and context lengths read, the scattered rows) over the device time per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--dtype fp16|bf16] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV GB/s (fraction of GB300 HBM peak); decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "llama3_8b_gqa"
+DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes the step must move at minimum.  Decode: K and V rows of the ctx
+    tokens of every (sequence, KV head), the query read and the output
+    written, the block-table entries the sequences reach and the context
+    lengths.  Scatter: the new K/V rows read and written and the slots."""
+    import numpy as np
+    s = w.elem_bytes
+    ctx = w.context_lens.numpy().astype(np.int64)
+    kv = int(2 * ctx.sum() * w.num_kv_heads * w.head_dim * s)
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * s
+    tables = int(4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * w.num_seqs)
+    T = int((w.slot_mapping.numpy() >= 0).sum())
+    scatter = 4 * T * w.num_kv_heads * w.head_dim * s + 8 * w.num_seqs
+    return {"kv": kv, "qo": qo, "tables": tables, "decode": kv + qo + tables,
+            "scatter": scatter, "step": kv + qo + tables + scatter}
+
+
+def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """K and V of one token over all layers: 2 * layers * kv_heads * d * bytes."""
+    return 2 * n_layers * n_kv_heads * head_dim * elem_bytes
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = x
+            walk(d)
+            for key in ("hbm_gbs", "hbm.gbs", "hbm_gbs_burst", "hbm.burst_gbs"):
+                if isinstance(flat.get(key), (int, float)):
+                    return float(flat[key]), f"measured (MEASURED_PEAKS.json {key})"
+            for k, v in flat.items():
+                if "hbm" in k.lower() and isinstance(v, (int, float)) and v > 100:
+                    return float(v), f"measured (MEASURED_PEAKS.json {k})"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "pagedattention_kv_cache_attention_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != decode_source_hash():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def make_workload(args):
+    import workloads
+    kw = {}
+    if args.dtype:
+        kw["dtype"] = args.dtype
+    return workloads.make(args.workload, seed=args.seed, **kw)
+
+
+def cpu_oracle_run(w, budget_s: float):
+    """Time the oracle (scatter + fp64 decode) on a bounded sample: the first
+    n sequences, n grown until one run takes a good part of the budget.
+    Returns (GB/s, cores, sample description, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
+    vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
+    cores = oracle.max_threads()
+    n = min(w.num_seqs, 4)
+    while True:
+        sub = slice(0, n)
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub])
+        oracle.decode(w.query[sub], kh, vh, w.block_tables[sub], w.context_lens[sub], w.scale,
+                      w.dtype, partition_size=w.partition_size)
+        dt = time.perf_counter() - t0
+        if n >= w.num_seqs or dt > budget_s / 4:
+            break
+        n = min(w.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 3) / max(dt, 1e-3)))))
+    ctx = w.context_lens.numpy()[:n].astype(np.int64)
+    s = w.elem_bytes
+    byts = (2 * ctx.sum() * w.num_kv_heads * w.head_dim * s
+            + 2 * n * w.num_q_heads * w.head_dim * s
+            + 4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * n
+            + 4 * n * w.num_kv_heads * w.head_dim * s + 8 * n)
+    sample = (f"first {n} of {w.num_seqs} sequences of {w.name} (all {w.num_q_heads} query heads, "
+              f"{int(ctx.sum())} context tokens), scatter + fp64 decode, one run of {dt:.2f} s")
+    return byts / dt / 1e9, cores, sample, dt, n
+
+
+def run_reference(args):
+    """The oracle as the reference arm, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = make_workload(args)
+    budget = 20.0 / max(1, args.steps + args.warmup)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, cores, sample, dt, n = cpu_oracle_run(w, max(budget, 2.0))
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic, seeded (numpy/torch CPU generators)",
+        "config": {"workload": w.name, "batch": w.num_seqs, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "partition_size": w.partition_size,
+                   "kv_dtype": w.dtype},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import pagedattention_kv_cache_attention_gb300 as pa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    w = make_workload(args)
+    ab = algorithmic_bytes(w)
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    key, value = w.key.to(dev), w.value.to(dev)
+    sm = w.slot_mapping.to(dev)
+    q = w.query.to(dev)
+    bt = w.block_tables.to(dev)
+    cl = w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    maxctx = w.max_context_len
+    ps = w.partition_size
+    nparts = pa.pa_decode_num_partitions(maxctx, ps)
+    ws = torch.empty(max(1, pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                        maxctx, ps)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.pa_reshape_and_cache(key, value, kc, vc, sm, stream=stream)
+        pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if pa.pa_device_errors(stream) != 0:
+        raise RuntimeError("device error bits raised during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for i in range(K):
+            pa.pa_reshape_and_cache(key, value, kc, vc, sm, stream=stream)
+            ev[i][0].record(stream)
+            pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_per_step = total_ms / K
+    if pa.pa_device_errors(stream) != 0:
+        raise RuntimeError("device error bits raised during the timed steps")
+
+    # end to end through the public API with host buffers: per step, pinned
+    # host -> device copies of the step's inputs, the step, and the output back
+    host = {n: t.pin_memory() for n, t in (("q", w.query), ("key", w.key), ("value", w.value),
+                                           ("sm", w.slot_mapping), ("bt", w.block_tables),
+                                           ("cl", w.context_lens))}
+    dq, dkey, dval = torch.empty_like(q), torch.empty_like(key), torch.empty_like(value)
+    dsm, dbt, dcl = torch.empty_like(sm), torch.empty_like(bt), torch.empty_like(cl)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dkey.copy_(host["key"], non_blocking=True)
+        dval.copy_(host["value"], non_blocking=True)
+        dsm.copy_(host["sm"], non_blocking=True)
+        dbt.copy_(host["bt"], non_blocking=True)
+        dcl.copy_(host["cl"], non_blocking=True)
+        pa.pa_reshape_and_cache(dkey, dval, kc, vc, dsm, stream=stream)
+        pa.pa_decode(out, dq, kc, vc, dbt, dcl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / K
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_src = hbm_peak()
+    achieved = ab["decode"] / (decode_ms * 1e-3) / 1e9
+    value_gbs = world * ab["step"] / (ms_per_step * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, sample, dt, n = cpu_oracle_run(w, args.cpu_budget)
+            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                   "sample": sample}
+        launches_per_step = 2 + (1 if nparts > 1 else 0)
+        line = {
+            "metric": METRIC,
+            "value": round(value_gbs, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16" if w.dtype == "fp16" else "bf16",
+            "data": "synthetic: seeded N(0,1) KV pool, queries and new tokens; NaN in every "
+                    "slot no sequence owns",
+            "config": {"workload": w.name, "batch": w.num_seqs, "q_heads": w.num_q_heads,
+                       "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "block_size": w.block_size, "num_blocks": w.num_blocks,
+                       "context_tokens": int(w.context_lens.sum()),
+                       "max_context_len": maxctx, "partition_size": ps,
+                       "partitions": nparts, "kv_dtype": w.dtype, "accumulate": "f32",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"no flush: inputs larger than L2 ({ab['kv'] / 1e6:.0f} MB of KV "
+                             f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2)"},
+            "decode_tokens_per_s": round(world * w.num_seqs / (ms_per_step * 1e-3), 1),
+            "hbm_fraction": round(value_gbs / world / peak, 4),
+            "bytes_per_step": ab,
+            "roofline": {"bound": "hbm", "kernel": "pa_decode (main kernel + LSE reduce)",
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": profiled_traffic(w.name), "peak_source": peak_src,
+                         "decode_ms": round(decode_ms, 5)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * ab["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--dtype", choices=("fp16", "bf16"), default=None)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of host time for the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

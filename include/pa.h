@@ -1,0 +1,188 @@
+/*
+ * pa.h -- C ABI of the PagedAttention decode library (libpa.so, sm_103a).
+ *
+ * The problem, as the pages state it:
+ *  - "LLM Serving Engine Shootout: vLLM vs TensorRT-LLM vs SGLang vs
+ *    llama.cpp", 3.1 PagedAttention Mechanics: each sequence's KV cache lives
+ *    in fixed-size physical blocks (16 or 32 tokens) of one pool; a block table
+ *    maps logical block index to physical block; the logit of the query against
+ *    key j is q . k_j / sqrt(d_head), with k_j fetched through
+ *    BlockTable[floor(j / block_size)].
+ *  - zhichai.net (Chinese original), section 1 diagram: tokens 0-15 of a
+ *    sequence in physical block #7, tokens 16-31 in physical block #2; token j
+ *    sits at row j mod block_size of its block.
+ *  - "Serving engines" (inference.tusharamrit.in), How vLLM works: given a
+ *    block table and a slot mapping, the kernel gathers the right K/V vectors
+ *    from scattered memory; blocks may be shared by several sequences
+ *    (copy-on-write), and a write forks only the block being written.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; the caller owns all memory.  No call allocates
+ *    device memory or keeps state between calls, except a per-device error
+ *    word (see pa_device_errors).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every compute call only validates its arguments on the host,
+ *    enqueues kernels on `stream` and returns; results are ready when the
+ *    stream reaches that point.
+ *  - Layouts (row-major, element type given by `dtype`, 2 bytes each):
+ *      k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim]
+ *      query, out        [num_seqs, num_q_heads, head_dim]
+ *      block_tables      int32 [num_seqs, max_blocks_per_seq]; entry
+ *                        (i, b) is the physical block of logical block b of
+ *                        sequence i; entries past a sequence's last block are
+ *                        never read (-1 by convention)
+ *      context_lens      int32 [num_seqs]; tokens 0..context_lens[i]-1 of
+ *                        sequence i are attended to (the newest token included)
+ *  - Query head h reads KV head h / (num_q_heads / num_kv_heads) (contiguous
+ *    query-head groups).
+ *  - Errors: host-side checks happen before any launch and return
+ *    PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED with nothing enqueued.  A failed
+ *    launch returns PA_ERR_CUDA.  Data errors that only the device can see
+ *    (a block-table entry outside [0, num_blocks), a slot outside the pool, a
+ *    context length beyond the table or beyond max_context_len, a wait that
+ *    ran out of time) never trap: the kernel skips the bad access (masking
+ *    the tokens it would have read, or skipping the bad row), records a bit
+ *    in the device error word, and the caller reads it with
+ *    pa_device_errors.  No call aborts or throws.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, too-small workspace */
+    PA_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels are built for */
+    PA_ERR_CUDA = 3           /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_FP16 = 0,              /* IEEE binary16 */
+    PA_BF16 = 1               /* bfloat16 */
+} pa_dtype;
+
+/* Bits of the device error word (see pa_device_errors). */
+#define PA_DEVERR_BAD_BLOCK 1u   /* a needed block-table entry was outside [0, num_blocks) */
+#define PA_DEVERR_BAD_SLOT  2u   /* a slot_mapping entry was >= num_blocks * block_size */
+#define PA_DEVERR_BAD_LEN   4u   /* a context length was < 0, > max_blocks_per_seq * block_size
+                                    or > max_context_len */
+#define PA_DEVERR_TIMEOUT   8u   /* a wait for staged KV data ran past its time limit */
+
+/*
+ * pa_reshape_and_cache -- write each new token's key and value into its slot
+ * of the paged cache ("Serving engines", How vLLM works: slot mapping).
+ *
+ *   for every t < num_tokens with s = slot_mapping[t] >= 0, every h:
+ *     k_cache[s / block_size, h, s % block_size, :] = key[t, h, :]
+ *     v_cache[s / block_size, h, s % block_size, :] = value[t, h, :]
+ *
+ * key, value       device, [num_tokens, num_kv_heads, head_dim]; row t starts
+ *                  at element t * key_stride (value_stride); heads are
+ *                  contiguous inside a row.  Strides in elements, >=
+ *                  num_kv_heads * head_dim and a multiple of 8.
+ * k_cache, v_cache device, updated in place; every other slot is untouched.
+ * slot_mapping     device int64 [num_tokens]; negative = skip the token.
+ * The copy is bit-exact.  Slots must be distinct within one call (two tokens
+ * writing one slot leave either value).  A slot >= num_blocks * block_size is
+ * skipped and sets PA_DEVERR_BAD_SLOT.
+ * Pointers 16-byte aligned.  head_dim in {64, 128}, block_size in {16, 32}.
+ */
+pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               int64_t key_stride, int64_t value_stride,
+                               void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               int32_t dtype, void *stream);
+
+/*
+ * Number of partitions pa_decode uses: 1 when partition_size == 0 or
+ * max_context_len <= partition_size, else ceil(max_context_len / partition_size).
+ */
+int32_t pa_decode_num_partitions(int32_t max_context_len, int32_t partition_size);
+
+/*
+ * Bytes of workspace pa_decode needs (0 when it runs as one partition).
+ * Layout, P = pa_decode_num_partitions(...), R = num_seqs * num_q_heads,
+ * each array starting at a 256-byte aligned offset, in this order:
+ *   m  float [R, P]      max over the partition of scale * q.k_j * log2(e)
+ *   l  float [R, P]      sum over the partition of 2^(scale*q.k_j*log2(e) - m)
+ *   o  float [R, P, head_dim]  the partition's normalised attention output
+ * Row r = seq * num_q_heads + head; only partitions p < ceil(ctx / partition_size)
+ * of a sequence are written.
+ */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                int32_t max_context_len, int32_t partition_size);
+
+/*
+ * pa_decode -- single-query paged attention for a batch of sequences
+ * ("LLM Serving Engine Shootout", 3.1 PagedAttention Mechanics).
+ *
+ *   out[i, h, :] = sum_j softmax_j(scale * q[i, h, :] . K_j) V_j,
+ *   j < context_lens[i], K_j = k_cache[block_tables[i, j / bs], h / G, j % bs, :]
+ *   (V_j alike), G = num_q_heads / num_kv_heads.  context_lens[i] == 0 gives 0.
+ *
+ * Softmax and accumulation are fp32 (online softmax in one pass over the
+ * tokens); out is rounded to dtype (round to nearest even).
+ * partition_size == 0, or max_context_len <= partition_size: one pass per
+ * (sequence, KV head) writes out directly; workspace may be NULL.
+ * partition_size > 0 (a multiple of 16): the tokens of each sequence are cut
+ * into partitions of partition_size, each partition is attended to
+ * separately into `workspace` (layout above), and pa_decode_reduce joins them
+ * by log-sum-exp on the same stream.
+ * max_context_len must be >= every context_lens[i] (sizes the launch).
+ * Pointers (out, query, caches) 16-byte aligned; head_dim in {64, 128};
+ * block_size in {16, 32}; num_q_heads / num_kv_heads in 1..8.
+ * The caches are read-only here; out must not overlap any input.
+ */
+pa_status pa_decode(void *out, const void *query,
+                    const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                    float scale, int32_t max_context_len, int32_t partition_size,
+                    void *workspace, size_t workspace_bytes,
+                    int32_t dtype, void *stream);
+
+/*
+ * pa_decode_reduce -- join split-context partitions by log-sum-exp:
+ *   M = max_p m_p,  w_p = l_p 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p
+ * over the ceil(context_lens[i] / partition_size) partitions of each row
+ * (0 partitions: out = 0).  `workspace` holds the partials in the layout of
+ * pa_decode_workspace_size for the same num_seqs, num_q_heads, head_dim,
+ * max_context_len and partition_size (partition_size > 0).  pa_decode calls
+ * this itself when it splits; it is exported so partials from elsewhere can
+ * be joined.
+ */
+pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                           int32_t max_context_len, int32_t partition_size,
+                           int32_t dtype, void *stream);
+
+/*
+ * Read and clear the device error word of the current device after waiting
+ * for `stream` to finish.  *flags receives the PA_DEVERR_* bits raised since
+ * the last call (by any call on any stream of this device).  Returns PA_OK or
+ * PA_ERR_CUDA.
+ */
+pa_status pa_device_errors(void *stream, uint32_t *flags);
+
+/* Static description of a status code (never NULL). */
+const char *pa_status_string(int32_t status);
+
+/* Library ABI version: 1. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,194 @@
+"""PagedAttention decode for GB300 (sm_103a): Python binding of libpa.
+
+The functions here carry the names of the C ABI in ``include/pa.h`` and do
+argument marshalling only: they check tensor devices, dtypes, shapes and
+contiguity, pass ``data_ptr()`` values, sizes and the current CUDA stream to
+the library, and turn a non-zero status into an exception.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback path, and
+importing a function fails loudly when ``libpa.so`` has not been built.
+
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
+    "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
+    "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
+]
+
+PA_FP16, PA_BF16 = 0, 1
+DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+_DT = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PaError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call}: {pa_status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise ImportError(
+                    f"libpa.so is not built ({_build.LIB} missing): run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            L = ctypes.CDLL(_build.LIB)
+            P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            L.pa_reshape_and_cache.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i64,
+                                               i32, P]
+            L.pa_reshape_and_cache.restype = i32
+            L.pa_decode_num_partitions.argtypes = [i32, i32]
+            L.pa_decode_num_partitions.restype = i32
+            L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            L.pa_decode_workspace_size.restype = sz
+            L.pa_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64,
+                                    ctypes.c_float, i32, i32, P, sz, i32, P]
+            L.pa_decode.restype = i32
+            L.pa_decode_reduce.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
+            L.pa_decode_reduce.restype = i32
+            L.pa_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.pa_device_errors.restype = i32
+            L.pa_status_string.argtypes = [i32]
+            L.pa_status_string.restype = ctypes.c_char_p
+            L.pa_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def pa_status_string(status: int) -> str:
+    return _load().pa_status_string(int(status)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(call: str, status: int) -> None:
+    if status != 0:
+        raise PaError(call, status)
+
+
+def _cuda(name: str, t: torch.Tensor, dtype=None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}: fp16 or bf16")
+    return _DT[t.dtype]
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write key/value [T, Hkv, d] rows into k_cache/v_cache [NB, Hkv, bs, d]
+    at slot_mapping[t] (int64; negative = skip), in place."""
+    for n, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, k_cache.dtype)
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("caches and slot_mapping must be contiguous")
+    T, Hkv, d = key.shape
+    NB, Hkv2, bs, d2 = k_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("key/value/cache shapes disagree")
+    if slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    for n, t in (("key", key), ("value", value)):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{n}: heads must be contiguous inside a token row")
+    _check("pa_reshape_and_cache", _load().pa_reshape_and_cache(
+        key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0), k_cache.data_ptr(),
+        v_cache.data_ptr(), slot_mapping.data_ptr(), T, Hkv, d, bs, NB, _dtype_code(k_cache),
+        _stream(stream)))
+
+
+def pa_decode_num_partitions(max_context_len: int, partition_size: int) -> int:
+    return int(_load().pa_decode_num_partitions(max_context_len, partition_size))
+
+
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+                             max_context_len: int, partition_size: int) -> int:
+    return int(_load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                                partition_size))
+
+
+def pa_decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+              scale: float, max_context_len: int, partition_size: int = 0,
+              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Paged decode attention into ``out`` [B, Hq, d].  ``workspace`` (a CUDA
+    uint8 tensor of pa_decode_workspace_size bytes) is allocated here with
+    torch when it is needed and not given."""
+    dt = k_cache.dtype
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, dt)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda("block_tables", block_tables, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    if not (block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("block_tables and context_lens must be contiguous")
+    B, Hq, d = query.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("out/query/cache shapes disagree")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    need = pa_decode_workspace_size(B, Hq, d, max_context_len, partition_size)
+    ws_ptr, ws_bytes = 0, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+        _cuda("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("pa_decode", _load().pa_decode(
+        out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, d,
+        bs, NB, float(scale), int(max_context_len), int(partition_size), ws_ptr or None,
+        ws_bytes, _dtype_code(k_cache), _stream(stream)))
+    return out
+
+
+def pa_decode_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: torch.Tensor,
+                     max_context_len: int, partition_size: int, stream=None) -> torch.Tensor:
+    """Join split-context partials in ``workspace`` into ``out`` [B, Hq, d]."""
+    _cuda("out", out)
+    _cuda("workspace", workspace)
+    _cuda("context_lens", context_lens, torch.int32)
+    B, Hq, d = out.shape
+    _check("pa_decode_reduce", _load().pa_decode_reduce(
+        out.data_ptr(), workspace.data_ptr(), context_lens.data_ptr(), B, Hq, d,
+        int(max_context_len), int(partition_size), _dtype_code(out), _stream(stream)))
+    return out
+
+
+def pa_device_errors(stream=None) -> int:
+    """Wait for ``stream`` and return (and clear) the device error bits."""
+    flags = ctypes.c_uint32(0)
+    _check("pa_device_errors", _load().pa_device_errors(_stream(stream), ctypes.byref(flags)))
+    return int(flags.value)

@@ -1,0 +1,529 @@
+// pa_decode.cu -- paged decode attention and the log-sum-exp partition join.
+//
+// What is computed ("LLM Serving Engine Shootout", 3.1 PagedAttention
+// Mechanics): for each sequence i and query head h, the logits
+// scale * q . k_j over the sequence's tokens j, with k_j (and v_j) read from
+// physical block BlockTable[i][j / block_size], row j % block_size (zhichai.net
+// section 1 diagram), a softmax over those logits, and the softmax-weighted
+// sum of the v_j.
+//
+// How (sm_103a):
+//  * One CTA per (KV head, sequence, partition).  It serves all G query heads
+//    of the KV head, so every K/V tile leaves HBM once per group.
+//  * The unit of work is a 16-token sub-tile: 16 consecutive rows of one
+//    physical block ([16, head_dim] contiguous in the pool layout
+//    [num_blocks, num_kv_heads, block_size, head_dim]).  Each warp owns a
+//    contiguous run of sub-tiles and a private ring of S shared-memory stages.
+//    Lane 0 of the warp loads each sub-tile's K and V with 2-D TMA copies
+//    (128-byte rows, 128-byte swizzle) through the block table, completion
+//    counted on one mbarrier per stage.  The warp's lanes keep the block ids
+//    of its next 32 sub-tiles in registers (one per lane), so the table lookup
+//    never sits on the issue path.
+//  * QK^T is a tensor-core contraction S^T[16 tokens, 8 heads] =
+//    K[16, d] Q^T[d, 8] (mma.sync m16n8k16, fp32 accumulate; the query group
+//    is padded to 8 heads).  The 16-byte K chunks a lane reads are chosen so
+//    that, with the 128-byte swizzle, every quarter-warp hits 32 distinct
+//    banks; Q is loaded once into registers in the matching order.
+//  * fp32 online softmax on the accumulator fragments (max over tokens by
+//    three butterfly shuffles; the running sum stays per thread until the end).
+//  * P.V is the second contraction O^T[d, 8] += V^T[d, 16] P^T[16, 8]: P is
+//    rounded to the KV dtype and moved into the B-operand layout by one 8x8
+//    transpose (movmatrix) per 8 tokens; V^T fragments are assembled from
+//    16-byte shared-memory reads with byte permutes.
+//  * Warps merge their (m, l, acc) through shared memory at the end.  Without
+//    a split the CTA writes the output; with a split it writes the
+//    partition's (m, l, normalised o) to the workspace and
+//    pa_decode_reduce_kernel joins partitions by log-sum-exp.
+//  * Tokens past the context length inside a sub-tile get logit -inf and a
+//    zeroed V row, so whatever those slots hold (even NaN) cannot reach the
+//    output.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kTile = 16;        // tokens per sub-tile (one MMA row block)
+constexpr int kBoxElems = 64;    // 128-byte TMA box width in 16-bit elements
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D> struct Shape {
+  static constexpr int kBoxes = D / kBoxElems;          // 128-byte boxes per row
+  static constexpr int kBoxBytes = kTile * 128;         // one box of 16 rows
+  static constexpr int kTileBytes = kTile * D * 2;      // K (or V) of one sub-tile
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+  static constexpr int kQChunks = D / 32;               // 16-byte q chunks per lane
+  static constexpr int kMTiles = D / 16;                // m16 tiles of the P.V product
+};
+
+// 16-byte chunk (8 elements) of a head_dim row that lane column c reads in
+// QK^T step i.  Every chunk is read by exactly one (i, c); chunks read by one
+// quarter-warp in one step are all even or all odd, which with the 128-byte
+// swizzle puts them in distinct banks.
+__device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
+
+template <typename T, int D, int NW, int S>
+__global__ void __launch_bounds__(NW * 32)
+    pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  using Sh = Shape<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzled TMA destinations need 1024-byte alignment.
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * Sh::kStageBytes);
+
+  const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+
+  int ctx = a.context_lens[seq];
+  if (ctx < 0 || ctx > (a.max_blocks_per_seq << a.bs_log2) || ctx > a.max_context_len) {
+    if (threadIdx.x == 0 && part == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
+    ctx = 0;
+  }
+  const int t_begin = part * a.part_tokens;
+  if (part > 0 && t_begin >= ctx) return;  // partition past the end: nothing to write
+  const int t_end = min(ctx, t_begin + a.part_tokens);
+  const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
+  const int per_warp = (n_sub + NW - 1) / NW;
+  const int w_begin = min(n_sub, warp * per_warp);
+  const int my_n = min(n_sub, w_begin + per_warp) - w_begin;
+
+  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
+  const int bs_mask = (1 << a.bs_log2) - 1;
+
+  // physical block of the warp's local sub-tile `k` (lane-parallel), -1 if
+  // past the run or invalid (invalid entries are flagged and masked)
+  auto block_id = [&](int k) -> int {
+    int phys = -1;
+    if (k < my_n) {
+      const int tok = t_begin + (w_begin + k) * kTile;
+      phys = bt_row[tok >> a.bs_log2];
+      if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
+        atomicOr(a.err, kErrBadBlock);
+        phys = -1;
+      }
+    }
+    return phys;
+  };
+
+  uint8_t *my_stages = smem + warp * S * Sh::kStageBytes;
+  uint64_t *my_bars = bars + warp * S;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const uint64_t policy = l2_policy_evict_first();
+  // lane 0: start loading local sub-tile k into stage s
+  auto issue = [&](int k, int phys, int s) {
+    uint64_t *bar = &my_bars[s];
+    if (phys >= 0) {
+      mbar_arrive_expect_tx(bar, Sh::kStageBytes);
+      const int tok = t_begin + (w_begin + k) * kTile;
+      const int y = ((phys * a.num_kv_heads + kvh) << a.bs_log2) + (tok & bs_mask);
+      uint8_t *st = my_stages + s * Sh::kStageBytes;
+#pragma unroll
+      for (int b = 0; b < Sh::kBoxes; ++b) {
+        tma_load_2d(st + b * Sh::kBoxBytes, &kmap, b * kBoxElems, y, bar, policy);
+        tma_load_2d(st + Sh::kTileBytes + b * Sh::kBoxBytes, &vmap, b * kBoxElems, y, bar,
+                    policy);
+      }
+    } else {
+      mbar_arrive(bar);  // nothing to load: complete the phase at once
+    }
+  };
+
+  // block ids of local sub-tiles [win_base, win_base + 32) and the next 32
+  int win_base = 0;
+  int win = block_id(lane);
+  int win_next = block_id(32 + lane);
+  uint32_t stage_ok = 0;  // bit s: the sub-tile in stage s has a valid block
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    if (s < my_n) {
+      const int phys = __shfl_sync(kFull, win, s);
+      stage_ok |= (phys >= 0 ? 1u : 0u) << s;
+      if (lane == 0) issue(s, phys, s);
+    }
+  }
+
+  // query fragments (B operand of S^T = K Q^T): head g, chunks q_chunk(i, c)
+  const int G = a.group;
+  uint4 qf[Sh::kQChunks];
+  {
+    const T *qrow = static_cast<const T *>(a.query) +
+                    (static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + g) * D;
+#pragma unroll
+    for (int i = 0; i < Sh::kQChunks; ++i)
+      qf[i] = g < G ? *reinterpret_cast<const uint4 *>(qrow + q_chunk(i, c) * 8)
+                    : make_uint4(0, 0, 0, 0);
+  }
+
+  const float NEG_INF = -INFINITY;
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;  // heads 2c, 2c+1
+  float acc[Sh::kMTiles][4];
+#pragma unroll
+  for (int mt = 0; mt < Sh::kMTiles; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+  bool timed_out = false;
+  int k_stop = my_n;
+#pragma unroll 1
+  for (int k = 0; k < my_n; ++k) {
+    const int s = k % S;
+    const uint32_t parity = (k / S) & 1;
+    const bool arrived = __all_sync(kFull, mbar_wait_bounded(&my_bars[s], parity));
+    if (!arrived) {
+      if (lane == 0) atomicOr(a.err, kErrTimeout);
+      timed_out = true;
+      k_stop = k;
+      break;
+    }
+    const bool ok = (stage_ok >> s) & 1u;
+    const int tok0 = t_begin + (w_begin + k) * kTile;
+    const int nvalid = ok ? min(kTile, t_end - tok0) : 0;
+    const uint8_t *Ks = my_stages + s * Sh::kStageBytes;
+    const uint8_t *Vs = Ks + Sh::kTileBytes;
+
+    // ---- S^T = K Q^T : rows g and g+8 (tokens), columns 2c, 2c+1 (heads)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < Sh::kQChunks; ++i) {
+      const int ch = q_chunk(i, c);
+      const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
+      const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
+      const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
+      const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
+      Elem<T>::mma(sc, ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
+      Elem<T>::mma(sc, ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
+    }
+
+    // ---- online softmax in base 2 (log2(e) folded into the scale)
+    const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
+    const float x0 = v_lo ? sc[0] * a.scale_log2 : NEG_INF;
+    const float x1 = v_lo ? sc[1] * a.scale_log2 : NEG_INF;
+    const float x2 = v_hi ? sc[2] * a.scale_log2 : NEG_INF;
+    const float x3 = v_hi ? sc[3] * a.scale_log2 : NEG_INF;
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float r0 = mn0 == NEG_INF ? 0.f : mn0;  // no valid token yet: any finite reference
+    const float r1 = mn1 == NEG_INF ? 0.f : mn1;
+    const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
+    const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1);
+    const float p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+    if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+    }
+    // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g)
+    const uint32_t pb0 = movmatrix_trans(Elem<T>::pack(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(Elem<T>::pack(p2, p3));
+
+    // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; chunk g of every box
+    uint4 v[4][Sh::kBoxes];
+#pragma unroll
+    for (int ri = 0; ri < 4; ++ri) {
+      const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
+      const bool keep = r < nvalid;
+#pragma unroll
+      for (int b = 0; b < Sh::kBoxes; ++b) {
+        const uint4 x =
+            *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 + ((g ^ (r & 7)) << 4));
+        v[ri][b] = keep ? x : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+      // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
+      constexpr int bA = 0;
+      constexpr int bB = Sh::kBoxes - 1;
+      const int eA = D == 128 ? mt : mt;
+      const int eB = D == 128 ? mt : 4 + mt;
+      const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
+      const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
+      const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
+      const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
+      Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+
+    // ---- refill this stage with local sub-tile k + S
+    __syncwarp();
+    const int nk = k + S;
+    if (nk < my_n) {
+      if (nk >= win_base + 32) {
+        win_base += 32;
+        win = win_next;
+        win_next = block_id(win_base + 32 + lane);
+      }
+      const int phys = __shfl_sync(kFull, win, nk - win_base);
+      stage_ok = (stage_ok & ~(1u << s)) | ((phys >= 0 ? 1u : 0u) << s);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(nk, phys, s);
+      }
+    }
+  }
+
+  if (timed_out) {
+    // let copies already in flight land before the CTA leaves (bounded again)
+    for (int kk = k_stop; kk < min(k_stop + S, my_n); ++kk)
+      (void)mbar_wait_bounded(&my_bars[kk % S], (kk / S) & 1);
+  }
+
+  // per-warp row sums over the 8 token rows (lanes differing in g)
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, off);
+    l1 += __shfl_xor_sync(kFull, l1, off);
+  }
+
+  // ---- merge warps through shared memory (stages are idle now)
+  __syncthreads();
+  float *wacc = reinterpret_cast<float *>(smem);  // [NW][8][D]
+  float *wml = wacc + NW * 8 * D;                 // [NW][8][2]
+  if (g == 0) {
+    wml[(warp * 8 + 2 * c) * 2 + 0] = m0;
+    wml[(warp * 8 + 2 * c) * 2 + 1] = l0;
+    wml[(warp * 8 + 2 * c + 1) * 2 + 0] = m1;
+    wml[(warp * 8 + 2 * c + 1) * 2 + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+    const int dA = D == 128 ? 8 * g + mt : 8 * g + mt;
+    const int dB = D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+    float *h0 = wacc + (warp * 8 + 2 * c) * D;
+    float *h1 = h0 + D;
+    h0[dA] = acc[mt][0];
+    h1[dA] = acc[mt][1];
+    h0[dB] = acc[mt][2];
+    h1[dB] = acc[mt][3];
+  }
+  __syncthreads();
+
+  constexpr int kChunks = D / 8;
+  for (int item = threadIdx.x; item < G * kChunks; item += NW * 32) {
+    const int h = item / kChunks, ch = item % kChunks;
+    float M = NEG_INF;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wml[(w * 8 + h) * 2]);
+    float L = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = wml[(w * 8 + h) * 2];
+      const float f = mw == NEG_INF ? 0.f : exp2f(mw - M);
+      L += wml[(w * 8 + h) * 2 + 1] * f;
+      const float *src = wacc + (w * 8 + h) * D + ch * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] += src[e] * f;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] *= inv;
+    const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h;
+    if (a.num_parts == 1) {
+      uint4 pk;
+      pk.x = Elem<T>::pack(o[0], o[1]);
+      pk.y = Elem<T>::pack(o[2], o[3]);
+      pk.z = Elem<T>::pack(o[4], o[5]);
+      pk.w = Elem<T>::pack(o[6], o[7]);
+      *reinterpret_cast<uint4 *>(static_cast<T *>(a.out) + row * D + ch * 8) = pk;
+    } else {
+      const int64_t pr = row * a.num_parts + part;
+      float4 *dst = reinterpret_cast<float4 *>(a.ws_o + pr * D + ch * 8);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+      if (ch == 0) {
+        a.ws_m[pr] = M;
+        a.ws_l[pr] = L;
+      }
+    }
+  }
+}
+
+// Log-sum-exp join of partitions: one CTA (4 warps) per (query head, sequence).
+template <typename T, int D>
+__global__ void __launch_bounds__(128) pa_decode_reduce_kernel(const ReduceArgs a) {
+  constexpr int NW = 4;
+  constexpr int kPer = D / 32;  // dims per lane
+  __shared__ float red_m[NW];
+  __shared__ float red_l[NW];
+  __shared__ float red_o[NW][D];
+  const int h = blockIdx.x, seq = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int ctx = a.context_lens[seq];
+  if (ctx < 0 || ctx > a.max_context_len) {
+    if (threadIdx.x == 0 && h == 0) atomicOr(a.err, kErrBadLen);
+    ctx = 0;
+  }
+  const int np = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 0;
+  const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h;
+  const float *m = a.ws_m + row * a.num_parts;
+  const float *l = a.ws_l + row * a.num_parts;
+  const float *o = a.ws_o + row * a.num_parts * D;
+
+  float M = -INFINITY;
+  for (int p = threadIdx.x; p < np; p += NW * 32) M = fmaxf(M, m[p]);
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
+
+  float L = 0.f, acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  if (M != -INFINITY) {
+    for (int p = warp; p < np; p += NW) {
+      const float mp = m[p];
+      const float f = mp == -INFINITY ? 0.f : l[p] * exp2f(mp - M);
+      L += f;
+      const float *op = o + static_cast<int64_t>(p) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(op);
+        acc[0] += f * x.x;
+        acc[1] += f * x.y;
+        acc[2] += f * x.z;
+        acc[3] += f * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2 *>(op);
+        acc[0] += f * x.x;
+        acc[1] += f * x.y;
+      }
+    }
+  }
+  if (lane == 0) red_l[warp] = L;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) red_o[warp][lane * kPer + e] = acc[e];
+  __syncthreads();
+  const float Lt = red_l[0] + red_l[1] + red_l[2] + red_l[3];
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+  for (int dd = threadIdx.x; dd < D / 2; dd += NW * 32) {
+    const int d0 = 2 * dd;
+    const float v0 = (red_o[0][d0] + red_o[1][d0] + red_o[2][d0] + red_o[3][d0]) * inv;
+    const float v1 = (red_o[0][d0 + 1] + red_o[1][d0 + 1] + red_o[2][d0 + 1] + red_o[3][d0 + 1]) * inv;
+    reinterpret_cast<uint32_t *>(static_cast<T *>(a.out) + row * D)[dd] = Elem<T>::pack(v0, v1);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The pool viewed as a 2-D tensor [num_blocks * num_kv_heads * block_size rows,
+// head_dim] loaded in boxes of 16 rows x 128 bytes with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxElems), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, const_cast<void *>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename T, int D, int NW, int S>
+cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+                            cudaStream_t stream) {
+  using Sh = Shape<D>;
+  constexpr size_t smem = 1024 + static_cast<size_t>(NW) * S * Sh::kStageBytes + NW * S * 8;
+  static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 <=
+                    static_cast<size_t>(NW) * S * Sh::kStageBytes,
+                "merge buffers must fit in the stage area");
+  auto kern = pa_decode_kernel<T, D, NW, S>;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  dim3 grid(a.num_parts, a.num_kv_heads, a.num_seqs);
+  kern<<<grid, NW * 32, smem, stream>>>(km, vm, a);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
+  dim3 grid(a.num_q_heads, a.num_seqs);
+  pa_decode_reduce_kernel<T, D><<<grid, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Warps per CTA and stages per warp of the decode kernel.
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+
+cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
+                          int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                          bool *map_failed) {
+  CUtensorMap km, vm;
+  *map_failed = false;
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype)) {
+    *map_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  if (dtype == 0) {
+    return head_dim == 128 ? launch_decode_t<__half, 128, kWarps, kStages>(a, km, vm, stream)
+                           : launch_decode_t<__half, 64, kWarps, kStages>(a, km, vm, stream);
+  }
+  return head_dim == 128 ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages>(a, km, vm, stream)
+                         : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages>(a, km, vm, stream);
+}
+
+cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream) {
+  if (dtype == 0)
+    return head_dim == 128 ? launch_reduce_t<__half, 128>(a, stream)
+                           : launch_reduce_t<__half, 64>(a, stream);
+  return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
+                         : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
+}
+
+}  // namespace pa

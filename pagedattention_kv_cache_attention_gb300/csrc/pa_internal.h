@@ -1,0 +1,52 @@
+// pa_internal.h -- argument blocks and launchers shared by the library's
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kMaxDevices = 64;
+
+struct DecodeArgs {
+  void *out;                    // [B, Hq, D] (used when num_parts == 1)
+  const void *query;            // [B, Hq, D]
+  const int32_t *block_tables;  // [B, max_blocks_per_seq]
+  const int32_t *context_lens;  // [B]
+  int max_blocks_per_seq;
+  int num_seqs, num_q_heads, num_kv_heads, group, bs_log2;
+  int64_t num_blocks;
+  float scale_log2;             // scale * log2(e)
+  int max_context_len;
+  int part_tokens;              // tokens per partition (>= max_context_len when not split)
+  int num_parts;
+  float *ws_m, *ws_l, *ws_o;    // split partials (num_parts > 1)
+  unsigned *err;                // device error word
+};
+
+struct ReduceArgs {
+  void *out;
+  const float *ws_m, *ws_l, *ws_o;
+  const int32_t *context_lens;
+  int num_seqs, num_q_heads, num_parts, partition_size, max_context_len;
+  unsigned *err;
+};
+
+struct ReshapeArgs {
+  const void *key, *value;
+  int64_t key_stride, value_stride;  // elements
+  void *k_cache, *v_cache;
+  const int64_t *slot_mapping;
+  int num_tokens, num_kv_heads, head_dim, block_size;
+  int64_t num_blocks;
+  unsigned *err;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
+                          int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                          bool *map_failed);
+cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
+cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
+
+}  // namespace pa
