@@ -27,9 +27,10 @@
 //  * fp32 online softmax on the accumulator fragments (max over tokens by
 //    three butterfly shuffles; the running sum stays per thread until the end).
 //  * P.V is the second contraction O^T[d, 8] += V^T[d, 16] P^T[16, 8]: P is
-//    rounded to the KV dtype and moved into the B-operand layout by one 8x8
-//    transpose (movmatrix) per 8 tokens; V^T fragments are assembled from
-//    16-byte shared-memory reads with byte permutes.
+//    split into hi + lo parts in the KV dtype (two MMAs, so P keeps ~16 or
+//    ~22 bits), each moved into the B-operand layout by an 8x8 transpose
+//    (movmatrix); V^T fragments are assembled from 16-byte shared-memory
+//    reads with byte permutes.
 //  * Warps merge their (m, l, acc) through shared memory at the end.  Without
 //    a split the CTA writes the output; with a split it writes the
 //    partition's (m, l, normalised o) to the workspace and
@@ -241,9 +242,16 @@ __global__ void __launch_bounds__(NW * 32)
         acc[mt][3] *= al1;
       }
     }
-    // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g)
-    const uint32_t pb0 = movmatrix_trans(Elem<T>::pack(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(Elem<T>::pack(p2, p3));
+    // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g).  P is
+    // carried as hi + lo in the KV dtype (hi = P rounded, lo = the exact fp32
+    // remainder rounded), so the P.V product keeps ~16 (bf16) or ~22 (fp16)
+    // bits of P instead of 8 or 11.
+    const uint32_t h01 = Elem<T>::pack(p0, p1), h23 = Elem<T>::pack(p2, p3);
+    const float2 f01 = Elem<T>::unpack(h01), f23 = Elem<T>::unpack(h23);
+    const uint32_t pb0 = movmatrix_trans(h01);
+    const uint32_t pb1 = movmatrix_trans(h23);
+    const uint32_t pr0 = movmatrix_trans(Elem<T>::pack(p0 - f01.x, p1 - f01.y));
+    const uint32_t pr1 = movmatrix_trans(Elem<T>::pack(p2 - f23.x, p3 - f23.y));
 
     // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; chunk g of every box
     uint4 v[4][Sh::kBoxes];
@@ -270,6 +278,7 @@ __global__ void __launch_bounds__(NW * 32)
       const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
       const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
       Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+      Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
     }
 
     // ---- refill this stage with local sub-tile k + S

@@ -105,7 +105,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
 }
 
 // Element types: packing two fp32 values into one 32-bit register (low half =
-// first value, round to nearest even) and the matching tensor-core MMA
+// first value, round to nearest even), unpacking, and the matching tensor-core MMA
 // D(16x8, fp32) += A(16x16) * B(16x8).
 template <typename T> struct Elem;
 
@@ -113,6 +113,9 @@ template <> struct Elem<__half> {
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
   }
   static __device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -128,6 +131,9 @@ template <> struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
   }
   static __device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -248,17 +248,17 @@ def test_reduce_alone_against_oracle_partials(pa):
 
 def test_bad_block_entry_is_flagged_not_read(pa):
     w = W.make("llama3_70b_cb", 7, lens=[100, 200, 64])
-    run_ok = Run(pa, w, partition_sizes=[0])
+    run_ok = Run(pa, w, partition_sizes=[0, 64])
     assert run_ok.err == 0
     bad = w.clone()
     bad.block_tables[1, 2] = w.num_blocks + 5      # outside the pool
     bad.block_tables[2, 0] = -3
     run = Run(pa, bad, partition_sizes=[0, 64])
     assert run.err & pa.DEVERR_BAD_BLOCK
-    for out in run.outs.values():
+    for ps, out in run.outs.items():
         assert torch.isfinite(out.float()).all()
-        # untouched sequence is still exact against the good run
-        assert torch.equal(out[0].view(torch.int16), run_ok.outs[0][0].view(torch.int16))
+        # the untouched sequence is bit-identical to the good run's
+        assert torch.equal(out[0].view(torch.int16), run_ok.outs[ps][0].view(torch.int16))
 
 
 def test_bad_slot_and_length_flags(pa):
