@@ -20,7 +20,8 @@
  *  - Pointers named as device pointers must point to device memory of the
  *    current CUDA device; the caller owns all memory.  No call allocates
  *    device memory or keeps state between calls, except a per-device error
- *    word (see pa_device_errors).
+ *    word (see pa_device_errors) and the fixed scratch array that
+ *    pa_decode_static_workspace uses.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every compute call only validates its arguments on the host,
  *    enqueues kernels on `stream` and returns; results are ready when the
@@ -166,6 +167,40 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
                            int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                            int32_t max_context_len, int32_t partition_size,
                            int32_t dtype, void *stream);
+
+/*
+ * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call: it exists for
+ * code that may not call cudaMalloc, such as work enqueued while a CUDA graph
+ * is being captured, host frameworks that have reserved all device memory for
+ * their own KV pool, or latency-critical enqueue paths that cannot afford an
+ * allocation's implicit device synchronisation.
+ *
+ * Same arguments and result as pa_decode, without workspace / workspace_bytes:
+ * the split-context partials go to a fixed array of PA_STATIC_WORKSPACE_BYTES
+ * inside the library (a __device__ variable, so every device that loads the
+ * library holds that much memory until the process exits).  The call allocates
+ * nothing and calls no allocating routine.
+ *  - A shape whose pa_decode_workspace_size exceeds PA_STATIC_WORKSPACE_BYTES
+ *    is rejected with PA_ERR_UNSUPPORTED before anything is enqueued.
+ *  - The first call on a device looks up that device's copy of the array
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents; no entry needs to start at zero.  Calls whose kernels overlap
+ *    on the GPU (different streams, or different host threads, without
+ *    ordering between them) race on the array: order them.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+pa_status pa_decode_static_workspace(void *out, const void *query,
+                                     const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *context_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     float scale, int32_t max_context_len, int32_t partition_size,
+                                     int32_t dtype, void *stream);
 
 /*
  * Read and clear the device error word of the current device after waiting

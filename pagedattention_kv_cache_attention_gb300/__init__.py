@@ -23,6 +23,7 @@ from . import build as _build
 __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
     "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
+    "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -184,6 +185,45 @@ def pa_decode_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: t
     _check("pa_decode_reduce", _load().pa_decode_reduce(
         out.data_ptr(), workspace.data_ptr(), context_lens.data_ptr(), B, Hq, d,
         int(max_context_len), int(partition_size), _dtype_code(out), _stream(stream)))
+    return out
+
+
+# Size of the library's own scratch array used by pa_decode_static_workspace
+# (PA_STATIC_WORKSPACE_BYTES in include/pa.h).
+STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024
+
+
+def pa_decode_static_workspace(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                               v_cache: torch.Tensor, block_tables: torch.Tensor,
+                               context_lens: torch.Tensor, scale: float, max_context_len: int,
+                               partition_size: int = 0, stream=None) -> torch.Tensor:
+    """pa_decode for callers that may not allocate device memory (work
+    enqueued during CUDA-graph capture, frameworks that have reserved all
+    device memory, enqueue paths that cannot afford an allocation's device
+    synchronisation): the split-context partials go to a fixed 64 MiB array
+    the library carries, so neither this binding nor the library allocates.
+    Shapes needing more scratch than that raise PaError (unsupported shape).
+    All calls on a device share the array; calls that overlap on the GPU race."""
+    L = _load()
+    if not getattr(L.pa_decode_static_workspace, "argtypes", None):
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                                 i64, ctypes.c_float, i32, i32, i32, P]
+        L.pa_decode_static_workspace.restype = i32
+    dt = k_cache.dtype
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, dt)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda("block_tables", block_tables, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    B, Hq, d = query.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    _check("pa_decode_static_workspace", L.pa_decode_static_workspace(
+        out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, d,
+        bs, NB, float(scale), int(max_context_len), int(partition_size), _dtype_code(k_cache),
+        _stream(stream)))
     return out
 
 

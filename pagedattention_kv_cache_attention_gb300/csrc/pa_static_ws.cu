@@ -1,0 +1,69 @@
+// pa_static_ws.cu -- pa_decode_static_workspace: paged decode for callers that
+// cannot allocate device memory.
+//
+// Some callers of this library may not call cudaMalloc: code that enqueues
+// work while a CUDA graph is being captured, host frameworks that have
+// reserved all device memory for their own KV pool and hand out no more, and
+// latency-critical enqueue paths where an allocation's implicit device-wide
+// synchronisation is not acceptable.  For them this entry point takes its
+// split-context scratch from a fixed array in device memory that the library
+// itself carries, instead of a caller-supplied workspace.
+//
+// The array is a file-scope __device__ variable: every device that loads the
+// library holds PA_STATIC_WORKSPACE_BYTES of it until the process exits.  In
+// host code its name only stands for the variable and is not a device
+// address, so the address is looked up once per device, with that device
+// current, by cudaGetSymbolAddress, and passed to the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+static __device__ __align__(256) unsigned char g_pa_static_workspace[PA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+std::mutex g_ws_mu;
+void *g_ws_ptr[pa::kMaxDevices] = {};
+
+// Device address of this device's copy of the array (first call per device
+// does the lookup).
+cudaError_t static_workspace(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= pa::kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  if (!g_ws_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pa_static_workspace);
+    if (e != cudaSuccess) return e;
+    g_ws_ptr[dev] = p;
+  }
+  *out = g_ws_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_static_workspace(
+    void *out, const void *query, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, float scale, int32_t max_context_len,
+    int32_t partition_size, int32_t dtype, void *stream) {
+  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                               partition_size);
+  if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_UNSUPPORTED;
+  void *ws = nullptr;
+  if (need > 0 && static_workspace(&ws) != cudaSuccess) return PA_ERR_CUDA;
+  // Every partial the kernels read is written earlier in the same call, so
+  // nothing in the array needs to start at zero.
+  return pa_decode(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                   num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                   max_context_len, partition_size, ws, need > 0 ? PA_STATIC_WORKSPACE_BYTES : 0,
+                   dtype, stream);
+}
