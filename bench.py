@@ -164,6 +164,8 @@ def make_workload(args):
     kw = {}
     if args.dtype:
         kw["dtype"] = args.dtype
+    if args.partition_size is not None:
+        kw["partition_size"] = args.partition_size
     return workloads.make(args.workload, seed=args.seed, **kw)
 
 
@@ -407,6 +409,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dtype", choices=("fp16", "bf16"), default=None)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--partition-size", type=int, default=None,
+                    help="override the workload's split-context partition (tokens, 0 = none)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of host time for the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

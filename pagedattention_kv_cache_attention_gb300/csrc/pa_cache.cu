@@ -6,7 +6,9 @@
 // [num_kv_heads, head_dim] K and V rows to
 // cache[slot / block_size, h, slot % block_size, :].  The copy is raw bytes,
 // so it is bit-exact for either 16-bit dtype.  A negative slot is skipped; a
-// slot past the pool is skipped and flagged.
+// slot past the pool is skipped and flagged.  It lets the next kernel in the
+// stream (the decode) start launching as soon as it begins; that kernel waits
+// for this one's writes before reading the pool.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -20,6 +22,8 @@ namespace {
 
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(const ReshapeArgs a) {
   const int t = blockIdx.x;
+  grid_dependency_wait();   // key/value/slots may come from the kernel before
+  grid_launch_dependents();  // the next kernel (decode) may start its set-up now
   const int64_t slot = a.slot_mapping[t];
   if (slot < 0) return;
   if (slot >= a.num_blocks * a.block_size) {
@@ -47,8 +51,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(const ReshapeArg
 }  // namespace
 
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream) {
-  reshape_and_cache_kernel<<<a.num_tokens, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(reshape_and_cache_kernel, dim3(a.num_tokens), dim3(128), 0, stream, a);
 }
 
 }  // namespace pa

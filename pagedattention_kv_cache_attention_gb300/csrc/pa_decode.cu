@@ -13,7 +13,8 @@
 //  * The unit of work is a 16-token sub-tile: 16 consecutive rows of one
 //    physical block ([16, head_dim] contiguous in the pool layout
 //    [num_blocks, num_kv_heads, block_size, head_dim]).  Each warp owns a
-//    contiguous run of sub-tiles and a private ring of S shared-memory stages.
+//    contiguous run of sub-tiles and a private ring of S shared-memory stages
+//    (4 warps x 2 stages: 64 KB per CTA, three CTAs per SM).
 //    Lane 0 of the warp loads each sub-tile's K and V with 2-D TMA copies
 //    (128-byte rows, 128-byte swizzle) through the block table, completion
 //    counted on one mbarrier per stage.  The warp's lanes keep the block ids
@@ -38,6 +39,11 @@
 //  * Tokens past the context length inside a sub-tile get logit -inf and a
 //    zeroed V row, so whatever those slots hold (even NaN) cannot reach the
 //    output.
+//  * Both kernels are launched as programmatic dependents of the previous
+//    kernel in the stream: the decode kernel sets up its barriers while the
+//    scatter finishes and waits (griddepcontrol.wait) before its first global
+//    read; the join waits for the decode grid, which lets it launch as its
+//    last CTAs finish.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -87,6 +93,18 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
 
+  uint8_t *my_stages = smem + warp * S * Sh::kStageBytes;
+  uint64_t *my_bars = bars + warp * S;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // inputs (the pool above all) may come from the kernel launched just before
+  grid_dependency_wait();
+
   int ctx = a.context_lens[seq];
   if (ctx < 0 || ctx > (a.max_blocks_per_seq << a.bs_log2) || ctx > a.max_context_len) {
     if (threadIdx.x == 0 && part == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
@@ -117,15 +135,6 @@ __global__ void __launch_bounds__(NW * 32)
     }
     return phys;
   };
-
-  uint8_t *my_stages = smem + warp * S * Sh::kStageBytes;
-  uint64_t *my_bars = bars + warp * S;
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
 
   const uint64_t policy = l2_policy_evict_first();
   // lane 0: start loading local sub-tile k into stage s
@@ -373,6 +382,7 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
+  grid_launch_dependents();
 }
 
 // Log-sum-exp join of partitions: one CTA (4 warps) per (query head, sequence).
@@ -385,6 +395,7 @@ __global__ void __launch_bounds__(128) pa_decode_reduce_kernel(const ReduceArgs 
   __shared__ float red_o[NW][D];
   const int h = blockIdx.x, seq = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();  // the partials come from the decode grid
   int ctx = a.context_lens[seq];
   if (ctx < 0 || ctx > a.max_context_len) {
     if (threadIdx.x == 0 && h == 0) atomicOr(a.err, kErrBadLen);
@@ -491,23 +502,27 @@ cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CU
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(a.num_parts, a.num_kv_heads, a.num_seqs);
-  kern<<<grid, NW * 32, smem, stream>>>(km, vm, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(a.num_parts, a.num_kv_heads, a.num_seqs), dim3(NW * 32),
+                          smem, stream, km, vm, a);
 }
 
 template <typename T, int D>
 cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
-  dim3 grid(a.num_q_heads, a.num_seqs);
-  pa_decode_reduce_kernel<T, D><<<grid, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(pa_decode_reduce_kernel<T, D>, dim3(a.num_q_heads, a.num_seqs),
+                          dim3(128), 0, stream, a);
 }
 
 }  // namespace
 
-// Warps per CTA and stages per warp of the decode kernel.
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
+// Warps per CTA and TMA stages per warp of the decode kernel.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kStages = PA_DECODE_STAGES;
 
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,

@@ -80,6 +80,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Programmatic dependent launch.  wait: block until the grids this one
+// depends on have finished and their writes are visible (a no-op when the
+// launch has no such dependency).  launch_dependents: allow the next grid in
+// the stream to start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2 policy for data read exactly once (the KV stream).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

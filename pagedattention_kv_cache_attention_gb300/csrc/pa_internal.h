@@ -43,6 +43,25 @@ struct ReshapeArgs {
   unsigned *err;
 };
 
+// Launch `kern` on `stream` as a programmatic dependent of the work before it:
+// it may start while the previous kernel finishes, and must call
+// griddepcontrol.wait before reading anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
                           bool *map_failed);
