@@ -277,6 +277,6 @@ def make(name: str, seed: int = 0, *, dtype: Optional[str] = None, batch: Option
                           1, max_len or 16384).astype(np.int64)
         return _build(name, seed, dtype or "fp16", len(ctx), num_q_heads or 64, num_kv_heads or 8,
                       head_dim or 128, block_size or 32, ctx, 1.2,
-                      partition_size if partition_size is not None else 512, rng, gen,
+                      partition_size if partition_size is not None else 1024, rng, gen,
                       table_len=max_len or 16384)
     raise KeyError(f"unknown workload {name!r}; known: {NAMES}")
