@@ -452,6 +452,70 @@ def run_ours(args):
     return 0
 
 
+def run_block_ops(args):
+    """Bandwidth of the whole-block moves on the workload's pool: a
+    copy-on-write fork of many blocks (pa_copy_blocks, both caches) and a swap
+    of the first quarter of the sequences to a pinned host pool and back
+    (pa_swap_blocks, both caches).  Bytes = blocks x block bytes x 2 (read and
+    write) x 2 caches."""
+    import numpy as np
+    import torch
+
+    import pagedattention_kv_cache_attention_gb300 as pa
+    dev = torch.device("cuda", 0)
+    w = make_workload(args)
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    block_bytes = kc[0].numel() * kc.element_size()
+    rng = np.random.default_rng(args.seed)
+    K = args.steps
+    res = {}
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / K
+
+    n = min(4096, w.num_blocks // 2)
+    ids = rng.permutation(w.num_blocks)
+    m = torch.from_numpy(np.stack([ids[:n], ids[n:2 * n]], 1).astype(np.int64)).to(dev)
+    ms = timed(lambda: pa.pa_copy_blocks(kc, vc, m))
+    res["copy_blocks"] = {"blocks": n, "ms": round(ms, 5),
+                          "GBps": round(4 * n * block_bytes / (ms * 1e-3) / 1e9, 1)}
+    nblk = w.blocks_used()
+    victims = np.concatenate([w.block_tables[i, :int(nblk[i])].numpy()
+                              for i in range(max(1, w.num_seqs // 4))]).astype(np.int64)
+    nv = len(victims)
+    hk = torch.empty((nv,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_m = torch.from_numpy(np.stack([victims, np.arange(nv)], 1)).to(dev)
+    in_m = torch.from_numpy(np.stack([np.arange(nv), victims], 1)).to(dev)
+
+    def swap_out():
+        pa.pa_swap_blocks(kc, hk, out_m)
+        pa.pa_swap_blocks(vc, hv, out_m)
+
+    def swap_in():
+        pa.pa_swap_blocks(hk, kc, in_m)
+        pa.pa_swap_blocks(hv, vc, in_m)
+    for nm, fn in (("swap_out", swap_out), ("swap_in", swap_in)):
+        ms = timed(fn)
+        res[nm] = {"blocks": nv, "ms": round(ms, 5),
+                   "GBps": round(2 * nv * block_bytes / (ms * 1e-3) / 1e9, 1),
+                   "note": "GB/s counts each byte once (one side is host memory)"}
+    if pa.pa_device_errors() != 0:
+        raise RuntimeError("device error bits raised")
+    print(json.dumps({"op": "block_moves", "workload": w.name, "block_bytes": block_bytes,
+                      "steps": K, "results": res}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,10 +530,14 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of host time for the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=("step", "blocks"), default="step",
+                    help="step: the decode step (default); blocks: copy/swap block bandwidth")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "blocks":
+        return run_block_ops(args)
     return run_ours(args)
 
 

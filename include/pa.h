@@ -169,6 +169,50 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
                            int32_t dtype, void *stream);
 
 /*
+ * pa_copy_blocks -- copy-on-write fork of whole physical blocks ("Serving
+ * engines", How vLLM works: sequences share physical blocks until one writes;
+ * the write forks only the block being written).
+ *
+ *   for every k < num_pairs, with (s, d) = (block_mapping[2k], block_mapping[2k+1]):
+ *     k_cache[d, :, :, :] = k_cache[s, :, :, :];  v_cache[d] = v_cache[s]
+ *
+ * k_cache, v_cache  device, [num_blocks, num_kv_heads, block_size, head_dim],
+ *                   16-byte aligned; updated in place, bit-exact.
+ * block_mapping     device int64 [num_pairs, 2].  Destinations must be
+ *                   distinct and none may also be a source in the same call
+ *                   (otherwise the result is undefined).  A pair with an id
+ *                   outside [0, num_blocks) is skipped and sets
+ *                   PA_DEVERR_BAD_BLOCK.
+ * head_dim in {64, 128}, block_size in {16, 32}.
+ */
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, void *stream);
+
+/*
+ * pa_swap_blocks -- move whole blocks between two pools, typically the device
+ * pool and a pinned host pool ("Serving engines", How vLLM works: a preempted
+ * sequence's blocks are swapped out to host memory and back in later).
+ *
+ *   for every k < num_pairs: dst block block_mapping[2k+1] = src block block_mapping[2k]
+ *
+ * src, dst       each device memory, managed memory, or pinned host memory
+ *                (cudaHostAlloc / cudaHostRegister; the library reaches it
+ *                through its device-mapped address); pageable host memory is
+ *                refused with PA_ERR_INVALID_ARG.  Both 16-byte aligned; pool
+ *                i has blocks of block_bytes (a multiple of 16) laid out
+ *                back to back.  Call once for the K pool and once for V.
+ * block_mapping  int64 [num_pairs, 2] in device or pinned host memory;
+ *                destinations distinct; ids outside [0, src_num_blocks) or
+ *                [0, dst_num_blocks) skip the pair and set PA_DEVERR_BAD_BLOCK.
+ * The copy is one kernel on `stream`, bit-exact.  As with every call, host
+ * memory must stay valid until the stream has passed this point.
+ */
+pa_status pa_swap_blocks(const void *src, void *dst, const int64_t *block_mapping,
+                         int32_t num_pairs, int64_t block_bytes, int64_t src_num_blocks,
+                         int64_t dst_num_blocks, void *stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
  * device memory.  The pages have no counterpart to this call: it exists for
  * code that may not call cudaMalloc, such as work enqueued while a CUDA graph

@@ -182,5 +182,22 @@ def lse_combine(m: np.ndarray, l: np.ndarray, o: np.ndarray, nparts) -> np.ndarr
     return out
 
 
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_mapping) -> None:
+    """Copy-on-write fork ("Serving engines", How vLLM works: a write forks
+    only the block being written): for every (src, dst) row of block_mapping,
+    physical block dst of both caches becomes a copy of block src, all heads
+    and rows.  Every source is read before any destination is written."""
+    m = np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+    for cache in (k_cache, v_cache):
+        cache[m[:, 1]] = cache[m[:, 0]].copy()
+
+
+def swap_blocks(src: np.ndarray, dst: np.ndarray, block_mapping) -> None:
+    """Preemption by swapping ("Serving engines", How vLLM works: blocks move
+    to host memory and back): dst block m[k, 1] = src block m[k, 0]."""
+    m = np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+    dst[m[:, 1]] = src[m[:, 0]]
+
+
 def max_threads() -> int:
     return int(lib().pa_oracle_max_threads())

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
     "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
-    "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES",
+    "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -225,6 +225,59 @@ def pa_decode_static_workspace(out: torch.Tensor, query: torch.Tensor, k_cache: 
         bs, NB, float(scale), int(max_context_len), int(partition_size), _dtype_code(k_cache),
         _stream(stream)))
     return out
+
+
+def _blocks_fn(name: str, argtypes):
+    L = _load()
+    f = getattr(L, name)
+    if not getattr(f, "argtypes", None):
+        f.argtypes = argtypes
+        f.restype = ctypes.c_int32
+    return f
+
+
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
+                   stream=None) -> None:
+    """Copy-on-write fork: for each row (src, dst) of ``block_mapping`` (CUDA
+    int64 [n, 2]), physical block dst of both caches becomes a copy of block
+    src.  Destinations distinct and not also sources."""
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f = _blocks_fn("pa_copy_blocks", [P, P, P, i32, i32, i32, i32, i64, P])
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, k_cache.dtype)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda("block_mapping", block_mapping, torch.int64)
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be a contiguous [n, 2] tensor")
+    NB, Hkv, bs, d = k_cache.shape
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    _check("pa_copy_blocks", f(k_cache.data_ptr(), v_cache.data_ptr(), block_mapping.data_ptr(),
+                               block_mapping.shape[0], Hkv, d, bs, NB, _stream(stream)))
+
+
+def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Tensor,
+                   stream=None) -> None:
+    """Move whole blocks between pools [NB, ...] (one cache): dst block
+    mapping[k, 1] = src block mapping[k, 0].  Each of src, dst is a CUDA tensor
+    or a pinned CPU tensor; ``block_mapping`` is int64 [n, 2] on the GPU or in
+    pinned CPU memory.  The copy runs as one kernel on ``stream``."""
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f = _blocks_fn("pa_swap_blocks", [P, P, P, i32, i64, i64, i64, P])
+    for n, t in (("src", src), ("dst", dst), ("block_mapping", block_mapping)):
+        if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be a CUDA tensor or a pinned CPU tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [n, 2]")
+    if src.dtype != dst.dtype or src.shape[1:] != dst.shape[1:]:
+        raise ValueError("src and dst must have the same dtype and block shape")
+    block_bytes = src[0].numel() * src.element_size() if src.shape[0] else 0
+    _check("pa_swap_blocks", f(src.data_ptr(), dst.data_ptr(), block_mapping.data_ptr(),
+                               block_mapping.shape[0], block_bytes, src.shape[0], dst.shape[0],
+                               _stream(stream)))
 
 
 def pa_device_errors(stream=None) -> int:

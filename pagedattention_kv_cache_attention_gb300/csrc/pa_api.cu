@@ -232,6 +232,82 @@ pa_status pa_decode(void *out, const void *query, const void *k_cache, const voi
   return PA_OK;
 }
 
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, void *stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_mapping || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
+  pa::BlockCopyArgs a;
+  a.src[0] = k_cache;
+  a.src[1] = v_cache;
+  a.dst[0] = k_cache;
+  a.dst[1] = v_cache;
+  a.mapping = block_mapping;
+  a.num_pairs = num_pairs;
+  a.block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * 2;
+  a.src_blocks = num_blocks;
+  a.dst_blocks = num_blocks;
+  a.err = err;
+  return pa::launch_block_copy(a, 2, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+namespace {
+// Device-usable address of device, managed or pinned host memory; null for
+// memory the device cannot reach (pageable host memory that was not pinned).
+const void *device_view(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return p;
+    case cudaMemoryTypeHost:
+      return at.devicePointer;
+    default:
+      return nullptr;
+  }
+}
+}  // namespace
+
+pa_status pa_swap_blocks(const void *src, void *dst, const int64_t *block_mapping,
+                         int32_t num_pairs, int64_t block_bytes, int64_t src_num_blocks,
+                         int64_t dst_num_blocks, void *stream) {
+  if (num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 || src_num_blocks <= 0 ||
+      dst_num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!src || !dst || !block_mapping || !aligned16(src) || !aligned16(dst))
+    return PA_ERR_INVALID_ARG;
+  const void *s = device_view(src);
+  void *d = const_cast<void *>(device_view(dst));
+  const void *m = device_view(block_mapping);
+  if (!s || !d || !m) return PA_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
+  pa::BlockCopyArgs a;
+  a.src[0] = a.src[1] = s;
+  a.dst[0] = a.dst[1] = d;
+  a.mapping = static_cast<const int64_t *>(m);
+  a.num_pairs = num_pairs;
+  a.block_bytes = block_bytes;
+  a.src_blocks = src_num_blocks;
+  a.dst_blocks = dst_num_blocks;
+  a.err = err;
+  return pa::launch_block_copy(a, 1, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_device_errors(void *stream, uint32_t *flags) {
   if (!flags) return PA_ERR_INVALID_ARG;
   unsigned int *err = nullptr;

@@ -43,6 +43,16 @@ struct ReshapeArgs {
   unsigned *err;
 };
 
+struct BlockCopyArgs {
+  const void *src[2];           // per tensor: source pool (device or mapped host memory)
+  void *dst[2];                 // per tensor: destination pool
+  const int64_t *mapping;       // [num_pairs, 2] (source block, destination block)
+  int num_pairs;
+  int64_t block_bytes;          // bytes of one block (multiple of 16)
+  int64_t src_blocks, dst_blocks;
+  unsigned *err;
+};
+
 // Launch `kern` on `stream` as a programmatic dependent of the work before it:
 // it may start while the previous kernel finishes, and must call
 // griddepcontrol.wait before reading anything that kernel writes.
@@ -67,5 +77,6 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
                           bool *map_failed);
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
+cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStream_t stream);
 
 }  // namespace pa

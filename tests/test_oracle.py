@@ -359,6 +359,65 @@ def pin_waste_under_one_block():
         assert np.all(waste < w.block_size) and np.all(waste >= 0)
 
 
+def _fork_case():
+    """Two sequences of one tiny pool share every physical block; the second
+    then forks its last block into a free block and writes its new token there."""
+    w = W.make("tiny_mha", 16, lens=[40, 40], num_q_heads=2, num_kv_heads=2)
+    w.block_tables[1] = w.block_tables[0]
+    w.slot_mapping[1] = -1  # the shared slot of token 39 is written once, by sequence 0
+    kc, vc = _after_scatter(w)
+    return w, kc, vc
+
+
+def pin_copy_on_write_fork():
+    """[ENG] copy-on-write: the second sequence forks the shared block it is
+    about to write and writes its new token (position 40) into the fork.  The
+    other sequence's output is bit-identical to before, and the writer reads
+    the shared rows followed by its own new token."""
+    w, kc, vc = _fork_case()
+    before = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype)
+    last = int(w.block_tables[1, 2])
+    owned = set(w.block_tables[0].numpy().tolist())
+    free = next(b for b in range(w.num_blocks) if b not in owned)
+    oracle.copy_blocks(kc, vc, [[last, free]])
+    w.block_tables[1, 2] = free
+    new_k = (np.arange(2 * 64) % 7).astype(np.float16).reshape(1, 2, 64)
+    oracle.reshape_and_cache(new_k.view(np.uint16), new_k.view(np.uint16), kc, vc,
+                             np.array([free * 16 + 8], np.int64))
+    w.context_lens[1] = 41
+    after = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype)
+    assert np.array_equal(after[0], before[0])
+    for h in range(2):
+        rows0 = oracle.gather(kc, w.block_tables[0], 40, h, "fp16")
+        rows1 = oracle.gather(kc, w.block_tables[1], 41, h, "fp16")
+        assert np.array_equal(rows1[:40], rows0)
+        assert np.array_equal(rows1[40], new_k[0, h].astype(np.float64))
+
+
+def pin_swap_out_and_back():
+    """[ENG] preemption by swapping: a sequence's blocks moved to a host pool
+    and back into other physical ids, with its table remapped, decode to the
+    bit-identical output."""
+    w = W.make("llama3_70b_cb", 17, lens=[70, 5, 33, 300, 200], head_dim=64, num_q_heads=4,
+               num_kv_heads=2)
+    kc, vc = _after_scatter(w)
+    before = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype)
+    used = w.block_tables[0, :3].numpy().astype(np.int64)
+    host_k = np.zeros((8,) + kc.shape[1:], np.uint16)
+    host_v = np.zeros_like(host_k)
+    oracle.swap_blocks(kc, host_k, np.stack([used, np.arange(3)], 1))
+    oracle.swap_blocks(vc, host_v, np.stack([used, np.arange(3)], 1))
+    kc[used] = 0xFFFF  # the freed blocks are reused by someone else
+    vc[used] = 0xFFFF
+    owned = set(w.block_tables.numpy().ravel().tolist())
+    fresh = np.array([b for b in range(w.num_blocks) if b not in owned][:3], np.int64)
+    oracle.swap_blocks(host_k, kc, np.stack([np.arange(3), fresh], 1))
+    oracle.swap_blocks(host_v, vc, np.stack([np.arange(3), fresh], 1))
+    w.block_tables[0, :3] = torch.from_numpy(fresh.astype(np.int32))
+    after = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype)
+    assert np.array_equal(after, before)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
