@@ -12,8 +12,9 @@
 //    of the KV head, so every K/V tile leaves HBM once per group.
 //  * The unit of work is a 16-token sub-tile: 16 consecutive rows of one
 //    physical block ([16, head_dim] contiguous in the pool layout
-//    [num_blocks, num_kv_heads, block_size, head_dim]).  Each warp owns a
-//    contiguous run of sub-tiles and a private ring of S shared-memory stages
+//    [num_blocks, num_kv_heads, block_size, head_dim]).  Warp w of a CTA takes
+//    sub-tiles w, w + NW, ... of the partition and owns a private ring of S
+//    shared-memory stages
 //    (4 warps x 2 stages: 64 KB per CTA, three CTAs per SM).
 //    Lane 0 of the warp loads each sub-tile's K and V with 2-D TMA copies
 //    (128-byte rows, 128-byte swizzle) through the block table, completion
@@ -105,36 +106,42 @@ __global__ void __launch_bounds__(NW * 32)
   // inputs (the pool above all) may come from the kernel launched just before
   grid_dependency_wait();
 
+  // Warp w takes sub-tiles w, w + NW, w + 2 NW, ... of the partition, so the
+  // block ids of its first 32 can be read before the context length arrives
+  // (entries past the sequence are read from the table row but never used).
+  const int t_begin = part * a.part_tokens;
+  const int full_sub = (a.part_tokens + kTile - 1) / kTile;
+  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
+  const int bs_mask = (1 << a.bs_log2) - 1;
+  auto table_entry = [&](int k) -> int {
+    const int u = warp + k * NW;
+    if (u >= full_sub) return -1;
+    const int lb = (t_begin + u * kTile) >> a.bs_log2;
+    return lb < a.max_blocks_per_seq ? bt_row[lb] : -1;
+  };
+  int win = table_entry(lane);
+
   int ctx = a.context_lens[seq];
   if (ctx < 0 || ctx > (a.max_blocks_per_seq << a.bs_log2) || ctx > a.max_context_len) {
     if (threadIdx.x == 0 && part == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
     ctx = 0;
   }
-  const int t_begin = part * a.part_tokens;
   if (part > 0 && t_begin >= ctx) return;  // partition past the end: nothing to write
   const int t_end = min(ctx, t_begin + a.part_tokens);
   const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
-  const int per_warp = (n_sub + NW - 1) / NW;
-  const int w_begin = min(n_sub, warp * per_warp);
-  const int my_n = min(n_sub, w_begin + per_warp) - w_begin;
+  const int my_n = n_sub > warp ? (n_sub - warp + NW - 1) / NW : 0;  // this warp's sub-tiles
 
-  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
-  const int bs_mask = (1 << a.bs_log2) - 1;
-
-  // physical block of the warp's local sub-tile `k` (lane-parallel), -1 if
-  // past the run or invalid (invalid entries are flagged and masked)
-  auto block_id = [&](int k) -> int {
-    int phys = -1;
-    if (k < my_n) {
-      const int tok = t_begin + (w_begin + k) * kTile;
-      phys = bt_row[tok >> a.bs_log2];
-      if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
-        atomicOr(a.err, kErrBadBlock);
-        phys = -1;
-      }
+  // physical block of the warp's k-th sub-tile, -1 if past its run or invalid
+  // (an invalid entry is flagged and its tokens are masked)
+  auto checked = [&](int k, int phys) -> int {
+    if (k >= my_n) return -1;
+    if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
+      atomicOr(a.err, kErrBadBlock);
+      return -1;
     }
     return phys;
   };
+  auto tile_token = [&](int k) { return t_begin + (warp + k * NW) * kTile; };
 
   const uint64_t policy = l2_policy_evict_first();
   // lane 0: start loading local sub-tile k into stage s
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(NW * 32)
     uint64_t *bar = &my_bars[s];
     if (phys >= 0) {
       mbar_arrive_expect_tx(bar, Sh::kStageBytes);
-      const int tok = t_begin + (w_begin + k) * kTile;
+      const int tok = tile_token(k);
       const int y = ((phys * a.num_kv_heads + kvh) << a.bs_log2) + (tok & bs_mask);
       uint8_t *st = my_stages + s * Sh::kStageBytes;
 #pragma unroll
@@ -156,10 +163,10 @@ __global__ void __launch_bounds__(NW * 32)
     }
   };
 
-  // block ids of local sub-tiles [win_base, win_base + 32) and the next 32
+  // block ids of the warp's sub-tiles [win_base, win_base + 32) and the next 32
   int win_base = 0;
-  int win = block_id(lane);
-  int win_next = block_id(32 + lane);
+  win = checked(lane, win);
+  int win_next = my_n > 32 ? checked(32 + lane, table_entry(32 + lane)) : -1;
   uint32_t stage_ok = 0;  // bit s: the sub-tile in stage s has a valid block
 #pragma unroll
   for (int s = 0; s < S; ++s) {
@@ -202,7 +209,7 @@ __global__ void __launch_bounds__(NW * 32)
       break;
     }
     const bool ok = (stage_ok >> s) & 1u;
-    const int tok0 = t_begin + (w_begin + k) * kTile;
+    const int tok0 = tile_token(k);
     const int nvalid = ok ? min(kTile, t_end - tok0) : 0;
     const uint8_t *Ks = my_stages + s * Sh::kStageBytes;
     const uint8_t *Vs = Ks + Sh::kTileBytes;
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(NW * 32)
       if (nk >= win_base + 32) {
         win_base += 32;
         win = win_next;
-        win_next = block_id(win_base + 32 + lane);
+        win_next = checked(win_base + 32 + lane, table_entry(win_base + 32 + lane));
       }
       const int phys = __shfl_sync(kFull, win, nk - win_base);
       stage_ok = (stage_ok & ~(1u << s)) | ((phys >= 0 ? 1u : 0u) << s);
@@ -385,68 +392,79 @@ __global__ void __launch_bounds__(NW * 32)
   grid_launch_dependents();
 }
 
-// Log-sum-exp join of partitions: one CTA (4 warps) per (query head, sequence).
+// Log-sum-exp join of partitions: one warp per output row (sequence, query
+// head), four rows per CTA.  Lanes read the partitions' (m, l) 32 at a time and
+// turn them into weights l_p 2^(m_p - M); every lane then accumulates its
+// head_dim / 32 output elements over the partitions' o rows.
+constexpr int kReduceRows = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) pa_decode_reduce_kernel(const ReduceArgs a) {
-  constexpr int NW = 4;
-  constexpr int kPer = D / 32;  // dims per lane
-  __shared__ float red_m[NW];
-  __shared__ float red_l[NW];
-  __shared__ float red_o[NW][D];
-  const int h = blockIdx.x, seq = blockIdx.y;
+__global__ void __launch_bounds__(kReduceRows * 32) pa_decode_reduce_kernel(const ReduceArgs a) {
+  constexpr int kPer = D / 32;  // output elements per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kReduceRows + warp;
   grid_dependency_wait();  // the partials come from the decode grid
+  if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
+  const int seq = static_cast<int>(row / a.num_q_heads);
   int ctx = a.context_lens[seq];
   if (ctx < 0 || ctx > a.max_context_len) {
-    if (threadIdx.x == 0 && h == 0) atomicOr(a.err, kErrBadLen);
+    if (lane == 0 && row % a.num_q_heads == 0) atomicOr(a.err, kErrBadLen);
     ctx = 0;
   }
   const int np = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 0;
-  const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h;
   const float *m = a.ws_m + row * a.num_parts;
   const float *l = a.ws_l + row * a.num_parts;
-  const float *o = a.ws_o + row * a.num_parts * D;
+  const float *o = a.ws_o + row * a.num_parts * D + lane * kPer;
 
   float M = -INFINITY;
-  for (int p = threadIdx.x; p < np; p += NW * 32) M = fmaxf(M, m[p]);
+  for (int p = lane; p < np; p += 32) M = fmaxf(M, m[p]);
+#pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  if (lane == 0) red_m[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
 
-  float L = 0.f, acc[kPer];
+  float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  if (M != -INFINITY) {
-    for (int p = warp; p < np; p += NW) {
+  float L = 0.f;
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    const int p = p0 + lane;
+    float wgt = 0.f;
+    if (p < np) {
       const float mp = m[p];
-      const float f = mp == -INFINITY ? 0.f : l[p] * exp2f(mp - M);
-      L += f;
-      const float *op = o + static_cast<int64_t>(p) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(op);
-        acc[0] += f * x.x;
-        acc[1] += f * x.y;
-        acc[2] += f * x.z;
-        acc[3] += f * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2 *>(op);
-        acc[0] += f * x.x;
-        acc[1] += f * x.y;
+      wgt = mp == -INFINITY ? 0.f : l[p] * exp2f(mp - M);
+    }
+    L += wgt;
+    const int cnt = min(32, np - p0);
+    int j = 0;
+    for (; j + 4 <= cnt; j += 4) {
+      float x[4][kPer];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) x[u][e] = o[static_cast<int64_t>(p0 + j + u) * D + e];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wj = __shfl_sync(kFull, wgt, j + u);
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] += wj * x[u][e];
       }
     }
-  }
-  if (lane == 0) red_l[warp] = L;
+    for (; j < cnt; ++j) {
+      const float wj = __shfl_sync(kFull, wgt, j);
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) red_o[warp][lane * kPer + e] = acc[e];
-  __syncthreads();
-  const float Lt = red_l[0] + red_l[1] + red_l[2] + red_l[3];
-  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-  for (int dd = threadIdx.x; dd < D / 2; dd += NW * 32) {
-    const int d0 = 2 * dd;
-    const float v0 = (red_o[0][d0] + red_o[1][d0] + red_o[2][d0] + red_o[3][d0]) * inv;
-    const float v1 = (red_o[0][d0 + 1] + red_o[1][d0 + 1] + red_o[2][d0 + 1] + red_o[3][d0 + 1]) * inv;
-    reinterpret_cast<uint32_t *>(static_cast<T *>(a.out) + row * D)[dd] = Elem<T>::pack(v0, v1);
+      for (int e = 0; e < kPer; ++e) acc[e] += wj * o[static_cast<int64_t>(p0 + j) * D + e];
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint32_t packed[kPer / 2];
+#pragma unroll
+  for (int e = 0; e < kPer / 2; ++e) packed[e] = Elem<T>::pack(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  T *dst = static_cast<T *>(a.out) + row * D + lane * kPer;
+  if constexpr (kPer == 4) {
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+  } else {
+    *reinterpret_cast<uint32_t *>(dst) = packed[0];
   }
 }
 
@@ -508,8 +526,10 @@ cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CU
 
 template <typename T, int D>
 cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
-  return launch_dependent(pa_decode_reduce_kernel<T, D>, dim3(a.num_q_heads, a.num_seqs),
-                          dim3(128), 0, stream, a);
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  return launch_dependent(pa_decode_reduce_kernel<T, D>,
+                          dim3(static_cast<unsigned>((rows + kReduceRows - 1) / kReduceRows)),
+                          dim3(kReduceRows * 32), 0, stream, a);
 }
 
 }  // namespace
