@@ -47,13 +47,14 @@ def algorithmic_bytes(w) -> dict:
     written, the block-table entries the sequences reach and the context
     lengths.  Scatter: the new K/V rows read and written and the slots."""
     import numpy as np
-    s = w.elem_bytes
+    s = w.elem_bytes  # cached element: 2 (fp16/bf16) or 1 (FP8)
     ctx = w.context_lens.numpy().astype(np.int64)
     kv = int(2 * ctx.sum() * w.num_kv_heads * w.head_dim * s)
-    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * s
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
     tables = int(4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * w.num_seqs)
     T = int((w.slot_mapping.numpy() >= 0).sum())
-    scatter = 4 * T * w.num_kv_heads * w.head_dim * s + 8 * w.num_seqs
+    # K and V rows: 16-bit values read, cached elements written
+    scatter = 2 * T * w.num_kv_heads * w.head_dim * (2 + s) + 8 * w.num_seqs
     return {"kv": kv, "qo": qo, "tables": tables, "decode": kv + qo + tables,
             "scatter": scatter, "step": kv + qo + tables + scatter}
 
@@ -182,7 +183,10 @@ def make_workload(args):
         kw["dtype"] = args.dtype
     if args.partition_size is not None:
         kw["partition_size"] = args.partition_size
-    return workloads.make(args.workload, seed=args.seed, **kw)
+    w = workloads.make(args.workload, seed=args.seed, **kw)
+    if getattr(args, "kv_dtype", None) == "e4m3":
+        w = workloads.to_fp8(w)
+    return w
 
 
 def cpu_oracle_run(w, budget_s: float):
@@ -193,16 +197,25 @@ def cpu_oracle_run(w, budget_s: float):
     import torch
 
     import oracle
-    kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
-    vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
+    fp8 = w.kv_dtype == "e4m3"
+    if fp8:
+        kh, vh = w.k_cache.numpy().copy(), w.v_cache.numpy().copy()
+    else:
+        kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
+        vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
     cores = oracle.max_threads()
     n = min(w.num_seqs, 4)
     while True:
         sub = slice(0, n)
         t0 = time.perf_counter()
-        oracle.reshape_and_cache(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub])
+        if fp8:
+            oracle.reshape_and_cache_fp8(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub],
+                                         w.dtype, w.k_scale, w.v_scale)
+        else:
+            oracle.reshape_and_cache(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub])
         oracle.decode(w.query[sub], kh, vh, w.block_tables[sub], w.context_lens[sub], w.scale,
-                      w.dtype, partition_size=w.partition_size)
+                      w.dtype, partition_size=w.partition_size,
+                      kv_dtype="e4m3" if fp8 else None, k_scale=w.k_scale, v_scale=w.v_scale)
         dt = time.perf_counter() - t0
         if n >= w.num_seqs or dt > budget_s / 4:
             break
@@ -210,9 +223,9 @@ def cpu_oracle_run(w, budget_s: float):
     ctx = w.context_lens.numpy()[:n].astype(np.int64)
     s = w.elem_bytes
     byts = (2 * ctx.sum() * w.num_kv_heads * w.head_dim * s
-            + 2 * n * w.num_q_heads * w.head_dim * s
+            + 2 * n * w.num_q_heads * w.head_dim * 2
             + 4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * n
-            + 4 * n * w.num_kv_heads * w.head_dim * s + 8 * n)
+            + 2 * n * w.num_kv_heads * w.head_dim * (2 + s) + 8 * n)
     sample = (f"first {n} of {w.num_seqs} sequences of {w.name} (all {w.num_q_heads} query heads, "
               f"{int(ctx.sum())} context tokens), scatter + fp64 decode, one run of {dt:.2f} s")
     return byts / dt / 1e9, cores, sample, dt, n
@@ -283,9 +296,26 @@ def run_ours(args):
                      device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    fp8 = w.kv_dtype == "e4m3"
+
+    def scatter(k_new, v_new, slots, st):
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(k_new, v_new, kc, vc, slots, w.k_scale, w.v_scale,
+                                        stream=st)
+        else:
+            pa.pa_reshape_and_cache(k_new, v_new, kc, vc, slots, stream=st)
+
+    def decode(qq, tables, lens, st):
+        if fp8:
+            pa.pa_decode_fp8(out, qq, kc, vc, tables, lens, w.scale, w.k_scale, w.v_scale, maxctx,
+                             ps, workspace=ws, stream=st)
+        else:
+            pa.pa_decode(out, qq, kc, vc, tables, lens, w.scale, maxctx, ps, workspace=ws,
+                         stream=st)
+
     def step():
-        pa.pa_reshape_and_cache(key, value, kc, vc, sm, stream=stream)
-        pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+        scatter(key, value, sm, stream)
+        decode(q, bt, cl, stream)
 
     for _ in range(args.warmup):
         step()
@@ -319,7 +349,7 @@ def run_ours(args):
           for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
-        pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+        decode(q, bt, cl, stream)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -331,16 +361,15 @@ def run_ours(args):
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             for _ in range(2):
-                pa.pa_reshape_and_cache(key, value, kc, vc, sm, stream=side)
-                pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws,
-                             stream=side)
+                scatter(key, value, sm, side)
+                decode(q, bt, cl, side)
         stream.wait_stream(side)
         torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             cs = torch.cuda.current_stream(dev)
-            pa.pa_reshape_and_cache(key, value, kc, vc, sm, stream=cs)
-            pa.pa_decode(out, q, kc, vc, bt, cl, w.scale, maxctx, ps, workspace=ws, stream=cs)
+            scatter(key, value, sm, cs)
+            decode(q, bt, cl, cs)
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize(dev)
@@ -375,8 +404,8 @@ def run_ours(args):
         dsm.copy_(host["sm"], non_blocking=True)
         dbt.copy_(host["bt"], non_blocking=True)
         dcl.copy_(host["cl"], non_blocking=True)
-        pa.pa_reshape_and_cache(dkey, dval, kc, vc, dsm, stream=stream)
-        pa.pa_decode(out, dq, kc, vc, dbt, dcl, w.scale, maxctx, ps, workspace=ws, stream=stream)
+        scatter(dkey, dval, dsm, stream)
+        decode(dq, dbt, dcl, stream)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -414,7 +443,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16" if w.dtype == "fp16" else "bf16",
+            "dtype": ("f16" if w.dtype == "fp16" else "bf16") + ("+e4m3 kv" if fp8 else ""),
             "data": "synthetic: seeded N(0,1) KV pool, queries and new tokens; NaN in every "
                     "slot no sequence owns",
             "config": {"workload": w.name, "batch": w.num_seqs, "q_heads": w.num_q_heads,
@@ -422,7 +451,8 @@ def run_ours(args):
                        "block_size": w.block_size, "num_blocks": w.num_blocks,
                        "context_tokens": int(w.context_lens.sum()),
                        "max_context_len": maxctx, "partition_size": ps,
-                       "partitions": nparts, "kv_dtype": w.dtype, "accumulate": "f32",
+                       "partitions": nparts, "kv_dtype": w.kv_dtype or w.dtype,
+                       "accumulate": "f32",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": f"no flush: inputs larger than L2 ({ab['kv'] / 1e6:.0f} MB of KV "
                              f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2)"},
@@ -524,6 +554,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dtype", choices=("fp16", "bf16"), default=None)
+    ap.add_argument("--kv-dtype", choices=("same", "e4m3"), default="same",
+                    help="e4m3: FP8 KV cache (fp16 queries)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=None,
                     help="override the workload's split-context partition (tokens, 0 = none)")

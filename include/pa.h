@@ -169,6 +169,50 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
                            int32_t dtype, void *stream);
 
 /*
+ * FP8 KV cache.  The cache stores one byte per element, an FP8 E4M3 code
+ * (1 sign, 4 exponent bits with bias 7, 3 fraction bits, no infinities,
+ * largest magnitude 448), with one scale per cache: code e stands for
+ * k_scale * e (K) or v_scale * e (V).  This halves the KV bytes the decode
+ * reads (zhichai.net section 4 counts FP8 at 1 byte per element; "Serving
+ * engines" lists KV quantisation among the shared engine features).
+ * Layout [num_blocks, num_kv_heads, block_size, head_dim] as above, uint8.
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into FP8 caches: every
+ * element x of the new rows (src_dtype fp16 or bf16) is stored as the E4M3
+ * code of x / scale, the quotient an IEEE single-precision division, rounded
+ * to the nearest code (ties to even), magnitudes beyond 448 clamped to 448.
+ * k_scale, v_scale finite and > 0.  Other arguments as pa_reshape_and_cache.
+ */
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                   int64_t key_stride, int64_t value_stride,
+                                   void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping,
+                                   int32_t num_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                   int32_t src_dtype, float k_scale, float v_scale,
+                                   void *stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over FP8 caches: K_j = k_scale * e4m3(k code),
+ * V_j = v_scale * e4m3(v code).  Codes are converted exactly to fp16 in the
+ * kernel; k_scale joins the softmax scale and v_scale multiplies the output.
+ * query/out fp16 (dtype = PA_FP16; PA_BF16 returns PA_ERR_UNSUPPORTED),
+ * head_dim 128, block_size 16 or 32.  Workspace as for pa_decode.
+ */
+pa_status pa_decode_fp8(void *out, const void *query,
+                        const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                        const int32_t *context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                        float scale, float k_scale, float v_scale,
+                        int32_t max_context_len, int32_t partition_size,
+                        void *workspace, size_t workspace_bytes,
+                        int32_t dtype, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write fork of whole physical blocks ("Serving
  * engines", How vLLM works: sequences share physical blocks until one writes;
  * the write forks only the block being written).

@@ -26,8 +26,8 @@ _OUT = os.path.join(_HERE, "_build", "libpa_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FP16, BF16 = 0, 1
-DT = {"fp16": FP16, "bf16": BF16}
+FP16, BF16, E4M3 = 0, 1, 2
+DT = {"fp16": FP16, "bf16": BF16, "e4m3": E4M3}
 
 
 def build(force: bool = False) -> str:
@@ -52,10 +52,19 @@ def _load(path: str) -> ctypes.CDLL:
     L.pa_oracle_bf16_to_f64.restype = ctypes.c_double
     L.pa_oracle_reshape_and_cache.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i64]
     L.pa_oracle_reshape_and_cache.restype = i32
-    L.pa_oracle_gather.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, i32, i64]
+    L.pa_oracle_gather.argtypes = [P, P, i32, ctypes.c_double, P, i32, i32, i32, i32, i32,
+                                   i32, i64]
     L.pa_oracle_gather.restype = i32
     L.pa_oracle_decode.argtypes = [P, P, P, P, i32, P, P, P, P, i32, P, i32, i32, i32,
-                                   i32, i32, i64, ctypes.c_float, i32, P, i32, i32, i32]
+                                   i32, i32, i64, ctypes.c_float, i32, i32, ctypes.c_double,
+                                   ctypes.c_double, P, i32, i32, i32]
+    L.pa_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    L.pa_oracle_e4m3_to_f64.restype = ctypes.c_double
+    L.pa_oracle_e4m3_from_f32.argtypes = [ctypes.c_float]
+    L.pa_oracle_e4m3_from_f32.restype = ctypes.c_uint8
+    L.pa_oracle_reshape_and_cache_fp8.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32,
+                                                  i64, i32, ctypes.c_float, ctypes.c_float]
+    L.pa_oracle_reshape_and_cache_fp8.restype = i32
     L.pa_oracle_decode.restype = i32
     L.pa_oracle_lse_combine.argtypes = [P, P, P, P, P, i32, i32, i32]
     L.pa_oracle_lse_combine.restype = None
@@ -117,29 +126,43 @@ def reshape_and_cache(key, value, k_cache: np.ndarray, v_cache: np.ndarray, slot
         raise IndexError(f"oracle reshape_and_cache: status {rc}")
 
 
-def gather(cache, block_table_row, ctx: int, kv_head: int, dtype: str) -> np.ndarray:
+def _kv(x, dtype: str) -> np.ndarray:
+    """Raw storage of a cache: uint8 codes for E4M3, 16-bit words otherwise."""
+    if dtype == "e4m3":
+        if hasattr(x, "detach"):
+            import torch
+            x = x.detach().contiguous().view(torch.uint8).numpy()
+        return np.ascontiguousarray(x).view(np.uint8)
+    return _u16(x)
+
+
+def gather(cache, block_table_row, ctx: int, kv_head: int, dtype: str,
+           mult: float = 1.0) -> np.ndarray:
     """Contiguous fp64 [ctx, d] rows of one sequence's KV head, read through its
-    block table."""
-    c = _u16(cache)
+    block table (each element times ``mult``, the FP8 dequantisation scale)."""
+    c = _kv(cache, dtype)
     NB, Hkv, bs, d = c.shape
     bt = _i32(block_table_row)
     out = np.empty((max(ctx, 0), d), dtype=np.float64)
-    rc = lib().pa_oracle_gather(_p(out), _p(c), DT[dtype], _p(bt), bt.shape[0], ctx, Hkv,
-                                kv_head, d, bs, NB)
+    rc = lib().pa_oracle_gather(_p(out), _p(c), DT[dtype], float(mult), _p(bt), bt.shape[0],
+                                ctx, Hkv, kv_head, d, bs, NB)
     if rc:
         raise IndexError(f"oracle gather: status {rc}")
     return out
 
 
 def decode(query, k_cache, v_cache, block_tables, context_lens, scale: float, dtype: str,
-           pairs=None, partition_size: int = 0, threads: int = 0, return_partials: bool = False):
+           pairs=None, partition_size: int = 0, threads: int = 0, return_partials: bool = False,
+           kv_dtype: str = None, k_scale: float = 1.0, v_scale: float = 1.0):
     """fp64 decode attention.  Returns out [n, d] for the (seq, head) ``pairs``
     (default: all, shaped [B, Hq, d]).  With ``partition_size`` > 0 the
     result is computed partition-wise and joined by log-sum-exp; with
-    ``return_partials`` also returns (m, l, o) per partition."""
+    ``return_partials`` also returns (m, l, o) per partition.  ``kv_dtype``
+    "e4m3" reads uint8 caches whose codes stand for k_scale*e / v_scale*e."""
+    kv_dtype = kv_dtype or dtype
     q = _u16(query)
-    kc = _u16(k_cache)
-    vc = _u16(v_cache)
+    kc = _kv(k_cache, kv_dtype)
+    vc = _kv(v_cache, kv_dtype)
     bt = _i32(block_tables)
     cl = _i32(context_lens)
     B, Hq, d = q.shape
@@ -159,8 +182,8 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, scale: float, dt
     rc = lib().pa_oracle_decode(
         _p(out), _p(pm) if pm is not None else None, _p(pl) if pl is not None else None,
         _p(po) if po is not None else None, maxp, _p(q), _p(kc), _p(vc), _p(bt), MB, _p(cl),
-        B, Hq, Hkv, d, bs, NB, float(scale), DT[dtype],
-        _p(pr) if pr is not None else None, n, partition_size, threads)
+        B, Hq, Hkv, d, bs, NB, float(scale), DT[dtype], DT[kv_dtype], float(k_scale),
+        float(v_scale), _p(pr) if pr is not None else None, n, partition_size, threads)
     if rc:
         raise IndexError(f"oracle decode: status {rc}")
     if pr is None:
@@ -168,6 +191,40 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, scale: float, dt
     if return_partials:
         return out, pm, pl, po
     return out
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact value of each E4M3 code (the oracle's own decoder)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().pa_oracle_e4m3_to_f64
+    return np.fromiter((f(int(v)) for v in c.ravel()), dtype=np.float64,
+                       count=c.size).reshape(c.shape)
+
+
+def e4m3_from_f32(x) -> np.ndarray:
+    """Nearest E4M3 code of each float32 (ties to even, saturating at 448)."""
+    a = np.asarray(x, dtype=np.float32)
+    f = lib().pa_oracle_e4m3_from_f32
+    return np.fromiter((f(float(v)) for v in a.ravel()), dtype=np.uint8,
+                       count=a.size).reshape(a.shape)
+
+
+def reshape_and_cache_fp8(key, value, k_cache: np.ndarray, v_cache: np.ndarray, slot_mapping,
+                          dtype: str, k_scale: float, v_scale: float) -> None:
+    """Scatter the new tokens' rows into uint8 E4M3 caches in place, each
+    element stored as the code of float32(x) / scale."""
+    k = _u16(key)
+    v = _u16(value)
+    T, Hkv, d = k.shape
+    NB, _, bs, _ = k_cache.shape
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    sm = np.ascontiguousarray(slot_mapping.detach().numpy() if hasattr(slot_mapping, "detach")
+                              else slot_mapping, dtype=np.int64)
+    rc = lib().pa_oracle_reshape_and_cache_fp8(
+        _p(k), _p(v), Hkv * d, Hkv * d, _p(k_cache), _p(v_cache), _p(sm), T, Hkv, d, bs, NB,
+        DT[dtype], float(k_scale), float(v_scale))
+    if rc:
+        raise IndexError(f"oracle reshape_and_cache_fp8: status {rc}")
 
 
 def lse_combine(m: np.ndarray, l: np.ndarray, o: np.ndarray, nparts) -> np.ndarray:

@@ -42,7 +42,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_FP16 = 0, ORC_BF16 = 1 };
+enum { ORC_FP16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
 enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_BAD_INDEX = 4, ORC_NO_MEM = 5 };
 
 /* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
@@ -83,6 +83,72 @@ static double to_f64(uint16_t x, int dtype)
 }
 
 /*
+ * FP8 E4M3 (the "fn" variant: no infinities): 1 sign, 4 exponent (bias 7),
+ * 3 fraction bits; exponent 15 with fraction 111 is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448; subnormals are f * 2^-9.
+ * (KV-cache quantisation, FP8 = 1 byte per element: zhichai.net, section 4
+ * byte table; "Serving engines", quantisation of weights and increasingly KV.)
+ */
+double pa_oracle_e4m3_to_f64(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);                   /* subnormal: f * 2^(1-7-3) */
+    else
+        v = ldexp((double)(f + 8), e - 10);         /* (1.f) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/*
+ * Nearest E4M3 code to x, ties to the even code, magnitudes beyond 448
+ * clamped to 448 (saturating), NaN to NaN (0x7f with x's sign).
+ */
+uint8_t pa_oracle_e4m3_from_f32(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x))
+        return sign | 0x7f;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7e;
+    /* spacing of representable values around a: 2^(E-3) in binade 2^E
+       (E >= -6), 2^-9 for the subnormals below 2^-6 */
+    int E;
+    frexp(a, &E);           /* a = m * 2^E, m in [0.5, 1): binade exponent E-1 */
+    int be = E - 1;
+    double quantum = be >= -6 ? ldexp(1.0, be - 3) : ldexp(1.0, -9);
+    double q = a / quantum;          /* exact: quantum is a power of two */
+    double r = floor(q);
+    double frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) == 1.0))
+        r += 1.0;
+    double v = r * quantum;          /* at most 448: a < 448 rounds to 448 at most */
+    /* encode v exactly */
+    if (v == 0.0)
+        return sign;
+    if (v < ldexp(1.0, -6))
+        return sign | (uint8_t)(v / ldexp(1.0, -9));            /* subnormal */
+    int e2;
+    double m = frexp(v, &e2);        /* v = m * 2^e2, m in [0.5, 1) */
+    int exp_field = e2 - 1 + 7;
+    int frac_field = (int)((m * 2.0 - 1.0) * 8.0);
+    return sign | (uint8_t)(exp_field << 3) | (uint8_t)frac_field;
+}
+
+/* Element idx of a cache of the given storage type, times mult. */
+static double kv_value(const void *cache, int64_t idx, int dtype, double mult)
+{
+    if (dtype == ORC_E4M3)
+        return mult * pa_oracle_e4m3_to_f64(((const uint8_t *)cache)[idx]);
+    return mult * to_f64(((const uint16_t *)cache)[idx], dtype);
+}
+
+/*
  * reshape_and_cache: for every new token t whose slot s = slot_mapping[t] is
  * not negative, copy the raw 16-bit words of key[t, h, :] and value[t, h, :]
  * into k_cache[s / bs, h, s % bs, :] and v_cache[...] for every KV head h.
@@ -112,13 +178,48 @@ int pa_oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
 }
 
 /*
+ * reshape_and_cache into an E4M3 cache: like pa_oracle_reshape_and_cache, but
+ * every element x of the new rows (fp16/bf16 `dtype`) is stored as the E4M3
+ * code of (float)x / scale (an IEEE single-precision quotient), rounded to
+ * nearest even with saturation at 448.
+ */
+int pa_oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
+                                    int64_t key_stride, int64_t value_stride, uint8_t *k_cache,
+                                    uint8_t *v_cache, const int64_t *slot_mapping, int T, int Hkv,
+                                    int d, int bs, int64_t NB, int dtype, float k_scale,
+                                    float v_scale)
+{
+    for (int t = 0; t < T; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= NB * (int64_t)bs)
+            return ORC_BAD_INDEX;
+        int64_t blk = s / bs, off = s % bs;
+        for (int h = 0; h < Hkv; ++h) {
+            int64_t dst = ((blk * Hkv + h) * bs + off) * d;
+            for (int c = 0; c < d; ++c) {
+                volatile float kq = (float)to_f64(key[t * key_stride + (int64_t)h * d + c], dtype) / k_scale;
+                volatile float vq = (float)to_f64(value[t * value_stride + (int64_t)h * d + c], dtype) / v_scale;
+                k_cache[dst + c] = pa_oracle_e4m3_from_f32(kq);
+                v_cache[dst + c] = pa_oracle_e4m3_from_f32(vq);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/*
  * Gather the first ctx rows of one sequence's KV head `kvh` into a contiguous
  * fp64 array out[ctx][d]: row j comes from physical block bt_row[j / bs],
- * row j % bs of that block.  Returns ORC_BAD_INDEX if a needed table entry is
- * outside [0, NB) or beyond the table's width MB.
+ * row j % bs of that block; each element is its exact value times `mult`
+ * (the dequantisation scale of an FP8 cache, 1 otherwise).  Returns
+ * ORC_BAD_INDEX if a needed table entry is outside [0, NB) or beyond the
+ * table's width MB.
  */
-int pa_oracle_gather(double *out, const uint16_t *cache, int dtype, const int32_t *bt_row,
-                     int MB, int ctx, int Hkv, int kvh, int d, int bs, int64_t NB)
+int pa_oracle_gather(double *out, const void *cache, int dtype, double mult,
+                     const int32_t *bt_row, int MB, int ctx, int Hkv, int kvh, int d, int bs,
+                     int64_t NB)
 {
     for (int j = 0; j < ctx; ++j) {
         int lb = j / bs;
@@ -127,9 +228,9 @@ int pa_oracle_gather(double *out, const uint16_t *cache, int dtype, const int32_
         int64_t phys = bt_row[lb];
         if (phys < 0 || phys >= NB)
             return ORC_BAD_INDEX;
-        const uint16_t *row = cache + ((phys * Hkv + kvh) * bs + (j % bs)) * (int64_t)d;
+        int64_t row = ((phys * Hkv + kvh) * bs + (j % bs)) * (int64_t)d;
         for (int c = 0; c < d; ++c)
-            out[(int64_t)j * d + c] = to_f64(row[c], dtype);
+            out[(int64_t)j * d + c] = kv_value(cache, row + c, dtype, mult);
     }
     return ORC_OK;
 }
@@ -176,9 +277,11 @@ static void attend(double *o, double *m_out, double *l_out, const double *q, con
 /*
  * Decode attention for a list of (sequence, query head) pairs.
  *
- * query [B, Hq, d], k_cache/v_cache [NB, Hkv, bs, d], block_tables [B, MB]
- * int32 (-1 = unused), context_lens [B] int32.  pairs = 2*npairs ints
- * (seq, head); NULL means all B*Hq pairs in (seq, head) order.
+ * query [B, Hq, d] (dtype fp16/bf16), k_cache/v_cache [NB, Hkv, bs, d] of
+ * kv_dtype (fp16, bf16, or E4M3 whose element e stands for k_scale * e or
+ * v_scale * e), block_tables [B, MB] int32 (-1 = unused), context_lens [B]
+ * int32.  pairs = 2*npairs ints (seq, head); NULL means all B*Hq pairs in
+ * (seq, head) order.
  *
  * partition_size == 0: out[k, :] = softmax attention over all ctx tokens.
  * partition_size  > 0: the ctx tokens are cut into partitions of
@@ -193,11 +296,12 @@ static void attend(double *o, double *m_out, double *l_out, const double *q, con
  * ORC_BAD_INDEX or ORC_NO_MEM.
  */
 int pa_oracle_decode(double *out, double *part_m, double *part_l, double *part_o,
-                     int max_parts, const uint16_t *query, const uint16_t *k_cache,
-                     const uint16_t *v_cache, const int32_t *block_tables, int MB,
+                     int max_parts, const uint16_t *query, const void *k_cache,
+                     const void *v_cache, const int32_t *block_tables, int MB,
                      const int32_t *context_lens, int B, int Hq, int Hkv, int d, int bs,
-                     int64_t NB, float scale, int dtype, const int32_t *pairs, int npairs,
-                     int partition_size, int nthreads)
+                     int64_t NB, float scale, int dtype, int kv_dtype, double k_scale,
+                     double v_scale, const int32_t *pairs, int npairs, int partition_size,
+                     int nthreads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || bs <= 0 || partition_size < 0)
         return ORC_BAD_ARG;
@@ -236,9 +340,11 @@ int pa_oracle_decode(double *out, double *part_m, double *part_l, double *part_o
             continue;
         }
         const int32_t *bt_row = block_tables + (int64_t)i * MB;
-        int rc = pa_oracle_gather(K, k_cache, dtype, bt_row, MB, ctx, Hkv, kvh, d, bs, NB);
+        int rc = pa_oracle_gather(K, k_cache, kv_dtype, k_scale, bt_row, MB, ctx, Hkv, kvh, d,
+                                  bs, NB);
         if (rc == ORC_OK)
-            rc = pa_oracle_gather(V, v_cache, dtype, bt_row, MB, ctx, Hkv, kvh, d, bs, NB);
+            rc = pa_oracle_gather(V, v_cache, kv_dtype, v_scale, bt_row, MB, ctx, Hkv, kvh, d,
+                                  bs, NB);
         if (rc != ORC_OK) {
             free(K); free(V); free(q); free(s);
 #ifdef _OPENMP

@@ -24,6 +24,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
     "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
     "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -278,6 +279,69 @@ def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Te
     _check("pa_swap_blocks", f(src.data_ptr(), dst.data_ptr(), block_mapping.data_ptr(),
                                block_mapping.shape[0], block_bytes, src.shape[0], dst.shape[0],
                                _stream(stream)))
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                             v_scale: float, stream=None) -> None:
+    """Write key/value [T, Hkv, d] (fp16/bf16) into uint8 FP8 E4M3 caches
+    [NB, Hkv, bs, d] at slot_mapping[t], each element as the code of x/scale."""
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f = _blocks_fn("pa_reshape_and_cache_fp8", [P, P, i64, i64, P, P, P, i32, i32, i32, i32,
+                                                 i64, i32, f32, f32, P])
+    for n, t in (("key", key), ("value", value)):
+        _cuda(n, t, key.dtype)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n}: heads must be contiguous inside a token row")
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda("slot_mapping", slot_mapping, torch.int64)
+    T, Hkv, d = key.shape
+    NB, Hkv2, bs, d2 = k_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("key/value/cache shapes disagree")
+    _check("pa_reshape_and_cache_fp8", f(
+        key.data_ptr(), value.data_ptr(), key.stride(0), value.stride(0), k_cache.data_ptr(),
+        v_cache.data_ptr(), slot_mapping.data_ptr(), T, Hkv, d, bs, NB, _dtype_code(key),
+        float(k_scale), float(v_scale), _stream(stream)))
+
+
+def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                  scale: float, k_scale: float, v_scale: float, max_context_len: int,
+                  partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Paged decode attention over uint8 FP8 E4M3 caches (codes times
+    k_scale / v_scale) into ``out`` [B, Hq, d] (fp16 queries and output)."""
+    P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    f = _blocks_fn("pa_decode_fp8", [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f32,
+                                     f32, f32, i32, i32, P, sz, i32, P])
+    for n, t in (("out", out), ("query", query)):
+        _cuda(n, t, query.dtype)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda("block_tables", block_tables, torch.int32)
+    _cuda("context_lens", context_lens, torch.int32)
+    B, Hq, d = query.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    need = pa_decode_workspace_size(B, Hq, d, max_context_len, partition_size)
+    ws_ptr, ws_bytes = 0, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("pa_decode_fp8", f(
+        out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, d,
+        bs, NB, float(scale), float(k_scale), float(v_scale), int(max_context_len),
+        int(partition_size), ws_ptr or None, ws_bytes, _dtype_code(query), _stream(stream)))
+    return out
 
 
 def pa_device_errors(stream=None) -> int:

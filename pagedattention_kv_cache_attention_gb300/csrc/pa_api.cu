@@ -112,6 +112,9 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_s
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
   pa::ReshapeArgs a;
+  a.to_fp8 = false;
+  a.src_dtype = dtype;
+  a.k_scale = a.v_scale = 1.f;
   a.key = key;
   a.value = value;
   a.key_stride = key_stride;
@@ -163,13 +166,17 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
              : PA_ERR_CUDA;
 }
 
-pa_status pa_decode(void *out, const void *query, const void *k_cache, const void *v_cache,
-                    const int32_t *block_tables, int32_t max_blocks_per_seq,
-                    const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                    int64_t num_blocks, float scale, int32_t max_context_len,
-                    int32_t partition_size, void *workspace, size_t workspace_bytes,
-                    int32_t dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status decode_impl(void *out, const void *query, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int64_t num_blocks, float scale, int32_t max_context_len,
+                      int32_t partition_size, void *workspace, size_t workspace_bytes,
+                      int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0 ||
       !dtype_ok(dtype) || !std::isfinite(scale))
@@ -212,7 +219,8 @@ pa_status pa_decode(void *out, const void *query, const void *k_cache, const voi
   a.group = group;
   a.bs_log2 = block_size == 16 ? 4 : 5;
   a.num_blocks = num_blocks;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale_log2 = scale * 1.4426950408889634f * k_scale;
+  a.out_scale = v_scale;
   a.max_context_len = max_context_len;
   a.part_tokens = P > 1 ? partition_size : (max_context_len > 0 ? max_context_len : 1);
   a.num_parts = P;
@@ -223,13 +231,88 @@ pa_status pa_decode(void *out, const void *query, const void *k_cache, const voi
   a.err = err;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   bool map_failed = false;
-  if (pa::launch_decode(a, k_cache, v_cache, pool_rows, head_dim, dtype, st, &map_failed) !=
-      cudaSuccess)
+  if (pa::launch_decode(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8, st,
+                        &map_failed) != cudaSuccess)
     return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
   if (P > 1)
     return pa_decode_reduce(out, workspace, context_lens, num_seqs, num_q_heads, head_dim,
                             max_context_len, partition_size, dtype, stream);
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode(void *out, const void *query, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int64_t num_blocks, float scale, int32_t max_context_len,
+                    int32_t partition_size, void *workspace, size_t workspace_bytes,
+                    int32_t dtype, void *stream) {
+  return decode_impl(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, max_context_len, partition_size, workspace,
+                     workspace_bytes, dtype, false, 1.f, 1.f, stream);
+}
+
+pa_status pa_decode_fp8(void *out, const void *query, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                        const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int64_t num_blocks, float scale, float k_scale, float v_scale,
+                        int32_t max_context_len, int32_t partition_size, void *workspace,
+                        size_t workspace_bytes, int32_t dtype, void *stream) {
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
+      !(v_scale > 0.f) || dtype != PA_FP16 && dtype != PA_BF16)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_FP16 || head_dim != 128) return PA_ERR_UNSUPPORTED;
+  return decode_impl(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, max_context_len, partition_size, workspace,
+                     workspace_bytes, dtype, true, k_scale, v_scale, stream);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t key_stride,
+                                   int64_t value_stride, void *k_cache, void *v_cache,
+                                   const int64_t *slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, int32_t src_dtype, float k_scale,
+                                   float v_scale, void *stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0 || !dtype_ok(src_dtype) ||
+      !std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+    return PA_ERR_INVALID_ARG;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8)
+    return PA_ERR_INVALID_ARG;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
+  pa::ReshapeArgs a;
+  a.to_fp8 = true;
+  a.src_dtype = src_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.key = key;
+  a.value = value;
+  a.key_stride = key_stride;
+  a.value_stride = value_stride;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.err = err;
+  return pa::launch_reshape(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                  : PA_ERR_CUDA;
 }
 
 pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,

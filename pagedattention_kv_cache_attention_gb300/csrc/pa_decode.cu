@@ -61,29 +61,37 @@ namespace pa {
 namespace {
 
 constexpr int kTile = 16;        // tokens per sub-tile (one MMA row block)
-constexpr int kBoxElems = 64;    // 128-byte TMA box width in 16-bit elements
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int D> struct Shape {
-  static constexpr int kBoxes = D / kBoxElems;          // 128-byte boxes per row
-  static constexpr int kBoxBytes = kTile * 128;         // one box of 16 rows
-  static constexpr int kTileBytes = kTile * D * 2;      // K (or V) of one sub-tile
-  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
-  static constexpr int kQChunks = D / 32;               // 16-byte q chunks per lane
-  static constexpr int kMTiles = D / 16;                // m16 tiles of the P.V product
+// Geometry of one sub-tile in shared memory.  Rows are staged in 128-byte TMA
+// boxes (16 rows each) with the 128-byte swizzle: 16-byte unit u of row r sits
+// at unit u ^ (r & 7) of its 128-byte line.
+template <int D, bool F8> struct Shape {
+  static constexpr int kElem = F8 ? 1 : 2;               // bytes per cached element
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kBoxElems = 128 / kElem;          // elements per 128-byte box row
+  static constexpr int kBoxes = kRowBytes / 128;         // boxes per row
+  static constexpr int kBoxBytes = kTile * 128;          // one box of 16 rows
+  static constexpr int kTileBytes = kTile * kRowBytes;   // K (or V) of one sub-tile
+  static constexpr int kStageBytes = 2 * kTileBytes;     // K + V
+  static constexpr int kQChunks = D / 32;                // 16-byte q chunks per lane
+  static constexpr int kMTiles = D / 16;                 // m16 tiles of the P.V product
 };
 
-// 16-byte chunk (8 elements) of a head_dim row that lane column c reads in
-// QK^T step i.  Every chunk is read by exactly one (i, c); chunks read by one
-// quarter-warp in one step are all even or all odd, which with the 128-byte
-// swizzle puts them in distinct banks.
+// 16-bit caches: the 16-byte chunk (8 elements) of a head_dim row that lane
+// column c reads in QK^T step i.  Every chunk is read by exactly one (i, c);
+// chunks read by one quarter-warp in one step are all even or all odd, which
+// with the swizzle puts them in distinct banks.
 __device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
 
-template <typename T, int D, int NW, int S>
+// T: query/output type (and the MMA type); F8: the caches hold FP8 E4M3 codes
+// (T is then fp16), converted exactly to fp16 in registers.
+template <typename T, int D, int NW, int S, bool F8>
 __global__ void __launch_bounds__(NW * 32)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using Sh = Shape<D>;
+  using Sh = Shape<D, F8>;
+  static_assert(!F8 || (D == 128 && sizeof(T) == 2), "FP8 caches: head_dim 128, fp16 queries");
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled TMA destinations need 1024-byte alignment.
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -154,8 +162,8 @@ __global__ void __launch_bounds__(NW * 32)
       uint8_t *st = my_stages + s * Sh::kStageBytes;
 #pragma unroll
       for (int b = 0; b < Sh::kBoxes; ++b) {
-        tma_load_2d(st + b * Sh::kBoxBytes, &kmap, b * kBoxElems, y, bar, policy);
-        tma_load_2d(st + Sh::kTileBytes + b * Sh::kBoxBytes, &vmap, b * kBoxElems, y, bar,
+        tma_load_2d(st + b * Sh::kBoxBytes, &kmap, b * Sh::kBoxElems, y, bar, policy);
+        tma_load_2d(st + Sh::kTileBytes + b * Sh::kBoxBytes, &vmap, b * Sh::kBoxElems, y, bar,
                     policy);
       }
     } else {
@@ -177,16 +185,18 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
 
-  // query fragments (B operand of S^T = K Q^T): head g, chunks q_chunk(i, c)
+  // query fragments (B operand of S^T = K Q^T) of head g: 16-bit caches use
+  // chunks q_chunk(i, c); FP8 caches use 16-dim units 2c + j (two chunks each)
   const int G = a.group;
   uint4 qf[Sh::kQChunks];
   {
     const T *qrow = static_cast<const T *>(a.query) +
                     (static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + g) * D;
 #pragma unroll
-    for (int i = 0; i < Sh::kQChunks; ++i)
-      qf[i] = g < G ? *reinterpret_cast<const uint4 *>(qrow + q_chunk(i, c) * 8)
-                    : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < Sh::kQChunks; ++i) {
+      const int ch = F8 ? 2 * (2 * c + (i >> 1)) + (i & 1) : q_chunk(i, c);
+      qf[i] = g < G ? *reinterpret_cast<const uint4 *>(qrow + ch * 8) : make_uint4(0, 0, 0, 0);
+    }
   }
 
   const float NEG_INF = -INFINITY;
@@ -216,15 +226,33 @@ __global__ void __launch_bounds__(NW * 32)
 
     // ---- S^T = K Q^T : rows g and g+8 (tokens), columns 2c, 2c+1 (heads)
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!F8) {
 #pragma unroll
-    for (int i = 0; i < Sh::kQChunks; ++i) {
-      const int ch = q_chunk(i, c);
-      const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
-      const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
-      const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
-      const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
-      Elem<T>::mma(sc, ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
-      Elem<T>::mma(sc, ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
+      for (int i = 0; i < Sh::kQChunks; ++i) {
+        const int ch = q_chunk(i, c);
+        const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
+        const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
+        const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
+        const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
+        Elem<T>::mma(sc, ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
+        Elem<T>::mma(sc, ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
+      }
+    } else {
+      // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) {
+        const int sw = ((2 * c + j) ^ g) << 4;
+        uint32_t ka[8], kb[8];
+        e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + g * 128 + sw), ka);
+        e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + (g + 8) * 128 + sw), kb);
+        const uint32_t q[8] = {qf[2 * j].x, qf[2 * j].y, qf[2 * j].z, qf[2 * j].w,
+                               qf[2 * j + 1].x, qf[2 * j + 1].y, qf[2 * j + 1].z,
+                               qf[2 * j + 1].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          Elem<T>::mma(sc, ka[2 * t], kb[2 * t], ka[2 * t + 1], kb[2 * t + 1], q[2 * t],
+                       q[2 * t + 1]);
+      }
     }
 
     // ---- online softmax in base 2 (log2(e) folded into the scale)
@@ -269,32 +297,53 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t pr0 = movmatrix_trans(Elem<T>::pack(p0 - f01.x, p1 - f01.y));
     const uint32_t pr1 = movmatrix_trans(Elem<T>::pack(p2 - f23.x, p3 - f23.y));
 
-    // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; chunk g of every box
-    uint4 v[4][Sh::kBoxes];
+    // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; unit g of every box
+    if constexpr (!F8) {
+      uint4 v[4][Sh::kBoxes];
 #pragma unroll
-    for (int ri = 0; ri < 4; ++ri) {
-      const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
-      const bool keep = r < nvalid;
+      for (int ri = 0; ri < 4; ++ri) {
+        const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
+        const bool keep = r < nvalid;
 #pragma unroll
-      for (int b = 0; b < Sh::kBoxes; ++b) {
-        const uint4 x =
-            *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 + ((g ^ (r & 7)) << 4));
-        v[ri][b] = keep ? x : make_uint4(0, 0, 0, 0);
+        for (int b = 0; b < Sh::kBoxes; ++b) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 +
+                                                           ((g ^ (r & 7)) << 4));
+          v[ri][b] = keep ? x : make_uint4(0, 0, 0, 0);
+        }
       }
-    }
 #pragma unroll
-    for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-      // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
-      constexpr int bA = 0;
-      constexpr int bB = Sh::kBoxes - 1;
-      const int eA = D == 128 ? mt : mt;
-      const int eB = D == 128 ? mt : 4 + mt;
-      const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
-      const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
-      const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
-      const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
-      Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-      Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+        // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
+        constexpr int bA = 0;
+        constexpr int bB = Sh::kBoxes - 1;
+        const int eA = mt;
+        const int eB = D == 128 ? mt : 4 + mt;
+        const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
+        const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
+        const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
+        const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
+        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+      }
+    } else {
+      // unit g (dims 16g .. 16g+15) of each row, converted to fp16
+      uint32_t vh[4][8];
+#pragma unroll
+      for (int ri = 0; ri < 4; ++ri) {
+        const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
+        const uint4 x = *reinterpret_cast<const uint4 *>(Vs + r * 128 + ((g ^ (r & 7)) << 4));
+        e4m3x16_to_half(r < nvalid ? x : make_uint4(0, 0, 0, 0), vh[ri]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+        // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt
+        const uint32_t a0 = pair_of16(vh[0], vh[1], mt);
+        const uint32_t a1 = pair_of16(vh[0], vh[1], 8 + mt);
+        const uint32_t a2 = pair_of16(vh[2], vh[3], mt);
+        const uint32_t a3 = pair_of16(vh[2], vh[3], 8 + mt);
+        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+      }
     }
 
     // ---- refill this stage with local sub-tile k + S
@@ -340,8 +389,8 @@ __global__ void __launch_bounds__(NW * 32)
   }
 #pragma unroll
   for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-    const int dA = D == 128 ? 8 * g + mt : 8 * g + mt;
-    const int dB = D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+    const int dA = F8 ? 16 * g + mt : 8 * g + mt;
+    const int dB = F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
     float *h0 = wacc + (warp * 8 + 2 * c) * D;
     float *h1 = h0 + D;
     h0[dA] = acc[mt][0];
@@ -367,7 +416,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] += src[e] * f;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float inv = L > 0.f ? a.out_scale / L : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] *= inv;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h;
@@ -486,29 +535,33 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // The pool viewed as a 2-D tensor [num_blocks * num_kv_heads * block_size rows,
 // head_dim] loaded in boxes of 16 rows x 128 bytes with the 128-byte swizzle.
-bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype) {
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
+                     bool fp8) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  const int elem = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxElems), static_cast<cuuint32_t>(kTile)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(kTile)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   2, const_cast<void *>(pool), dims, strides, box, estr,
+  const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : (dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUresult r = enc(map, ty, 2, const_cast<void *>(pool), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <typename T, int D, int NW, int S>
+template <typename T, int D, int NW, int S, bool F8>
 cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                             cudaStream_t stream) {
-  using Sh = Shape<D>;
+  using Sh = Shape<D, F8>;
   constexpr size_t smem = 1024 + static_cast<size_t>(NW) * S * Sh::kStageBytes + NW * S * 8;
   static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 <=
                     static_cast<size_t>(NW) * S * Sh::kStageBytes,
                 "merge buffers must fit in the stage area");
-  auto kern = pa_decode_kernel<T, D, NW, S>;
+  auto kern = pa_decode_kernel<T, D, NW, S, F8>;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -544,22 +597,29 @@ cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
 constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStages = PA_DECODE_STAGES;
 
+// FP8 caches have half the bytes per stage: twice the stages keep as many
+// bytes in flight per warp.
+constexpr int kStagesF8 = 2 * kStages;
+
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
-                          int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                          bool *map_failed) {
+                          int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                          cudaStream_t stream, bool *map_failed) {
   CUtensorMap km, vm;
   *map_failed = false;
-  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype) ||
-      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype)) {
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, kv_fp8) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, kv_fp8)) {
     *map_failed = true;
     return cudaErrorInvalidValue;
   }
+  if (kv_fp8) return launch_decode_t<__half, 128, kWarps, kStagesF8, true>(a, km, vm, stream);
   if (dtype == 0) {
-    return head_dim == 128 ? launch_decode_t<__half, 128, kWarps, kStages>(a, km, vm, stream)
-                           : launch_decode_t<__half, 64, kWarps, kStages>(a, km, vm, stream);
+    return head_dim == 128
+               ? launch_decode_t<__half, 128, kWarps, kStages, false>(a, km, vm, stream)
+               : launch_decode_t<__half, 64, kWarps, kStages, false>(a, km, vm, stream);
   }
-  return head_dim == 128 ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages>(a, km, vm, stream)
-                         : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages>(a, km, vm, stream);
+  return head_dim == 128
+             ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages, false>(a, km, vm, stream)
+             : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages, false>(a, km, vm, stream);
 }
 
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream) {

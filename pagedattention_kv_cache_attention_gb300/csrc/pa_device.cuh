@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace pa {
@@ -164,6 +165,27 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 // half), where x and y each hold 8 consecutive 16-bit elements.
 __device__ __forceinline__ uint32_t pair_of(const uint4 &x, const uint4 &y, int e) {
   return __byte_perm(word_of(x, e >> 1), word_of(y, e >> 1), (e & 1) ? 0x7632 : 0x5410);
+}
+
+// 16 FP8 E4M3 values (one 16-byte load, element 0 in the lowest byte) to 8
+// words of fp16 pairs in the same order.  Every E4M3 value is exact in fp16.
+__device__ __forceinline__ void e4m3x16_to_half(const uint4 &x, uint32_t (&h)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+    h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+    h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+  }
+}
+
+// Elements e of two 16-element fp16 rows (8 words each): x's in the low half.
+__device__ __forceinline__ uint32_t pair_of16(const uint32_t (&x)[8], const uint32_t (&y)[8],
+                                              int e) {
+  return __byte_perm(x[e >> 1], y[e >> 1], (e & 1) ? 0x7632 : 0x5410);
 }
 
 }  // namespace pa

@@ -17,7 +17,8 @@ struct DecodeArgs {
   int max_blocks_per_seq;
   int num_seqs, num_q_heads, num_kv_heads, group, bs_log2;
   int64_t num_blocks;
-  float scale_log2;             // scale * log2(e)
+  float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
+  float out_scale;              // V dequantisation scale for FP8, 1 otherwise
   int max_context_len;
   int part_tokens;              // tokens per partition (>= max_context_len when not split)
   int num_parts;
@@ -34,6 +35,10 @@ struct ReduceArgs {
 };
 
 struct ReshapeArgs {
+  // FP8 caches: elements are stored as E4M3 codes of x / scale
+  bool to_fp8;
+  int src_dtype;                     // fp16 / bf16 source rows when to_fp8
+  float k_scale, v_scale;
   const void *key, *value;
   int64_t key_stride, value_stride;  // elements
   void *k_cache, *v_cache;
@@ -72,9 +77,10 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// kv_fp8: the caches hold FP8 E4M3 codes (queries and output fp16).
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
-                          int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                          bool *map_failed);
+                          int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                          cudaStream_t stream, bool *map_failed);
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
 cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStream_t stream);

@@ -418,6 +418,87 @@ def pin_swap_out_and_back():
     assert np.array_equal(after, before)
 
 
+# --------------------------------------------------------------- FP8 caches
+
+def pin_e4m3_decode_all_codes():
+    """The oracle's E4M3 decoder against torch's float8_e4m3fn on all 256 codes."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan) and nan.sum() == 2
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9
+
+
+def pin_e4m3_encode_matches_torch():
+    """Nearest code, ties to even: equal to torch's cast for every fp16 value
+    below the first magnitude torch turns into NaN (464), and for random
+    float32 values in range."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float32)
+    rng = np.random.default_rng(0)
+    x = np.concatenate([x, rng.uniform(-463, 463, 20000).astype(np.float32),
+                        rng.standard_normal(20000).astype(np.float32) * 1e-2])
+    x = x[np.isfinite(x) & (np.abs(x) < 464)]
+    mine = oracle.e4m3_from_f32(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+
+
+def pin_e4m3_saturates():
+    """Beyond the largest magnitude the encoder clamps to +-448 (saturating
+    conversion), NaN stays NaN."""
+    x = np.array([464.0, 470.0, 479.9, 480.0, 1e6, np.inf, -500.0, -np.inf, np.nan],
+                 dtype=np.float32)
+    got = oracle.e4m3_from_f32(x)
+    assert got.tolist()[:8] == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert got[8] & 0x7F == 0x7F
+
+
+def pin_fp8_scatter_codes():
+    """reshape_and_cache into FP8 caches stores code(float32(x) / scale) at the
+    slot (checked against torch's cast), and nothing else changes."""
+    w = W.make("llama3_8b_gqa", 18, batch=3, max_len=700)
+    f8 = W.to_fp8(w)
+    kc, vc = f8.k_cache.numpy().copy(), f8.v_cache.numpy().copy()
+    oracle.reshape_and_cache_fp8(w.key, w.value, kc, vc, w.slot_mapping, "fp16", f8.k_scale,
+                                 f8.v_scale)
+    changed = np.argwhere(kc != f8.k_cache.numpy())
+    for i in range(w.num_seqs):
+        s = int(w.slot_mapping[i])
+        blk, off = s // w.block_size, s % w.block_size
+        exp_k = (w.key[i].float() / torch.tensor(f8.k_scale, dtype=torch.float32)).clamp(-448, 448)
+        exp_k = exp_k.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(kc[blk, :, off, :], exp_k)
+        exp_v = (w.value[i].float() / torch.tensor(f8.v_scale, dtype=torch.float32)).clamp(-448, 448)
+        assert np.array_equal(vc[blk, :, off, :],
+                              exp_v.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    slots = {(int(s) // w.block_size, int(s) % w.block_size) for s in w.slot_mapping}
+    assert all((int(b), int(o)) in slots for b, _, o, _ in changed)
+
+
+def pin_fp8_decode_equals_16bit_when_exact():
+    """With power-of-two scales every dequantised element is exactly an fp16
+    value, so the FP8 decode must equal the fp16 decode of those values bit
+    for bit; a V scale multiplies the output; a K scale is a logit scale."""
+    w = W.make("llama3_8b_gqa", 19, lens=[3, 70, 260], head_dim=64, num_q_heads=8,
+               num_kv_heads=2)
+    f8 = W.to_fp8(w, k_scale=0.25, v_scale=0.5)
+    kc, vc = f8.k_cache.numpy().copy(), f8.v_cache.numpy().copy()
+    oracle.reshape_and_cache_fp8(w.key, w.value, kc, vc, w.slot_mapping, "fp16", 0.25, 0.5)
+    k16 = (torch.from_numpy(kc).view(torch.float8_e4m3fn).float() * 0.25).half()
+    v16 = (torch.from_numpy(vc).view(torch.float8_e4m3fn).float() * 0.5).half()
+    got = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, "fp16",
+                        kv_dtype="e4m3", k_scale=0.25, v_scale=0.5)
+    ref = oracle.decode(w.query, k16, v16, w.block_tables, w.context_lens, w.scale, "fp16")
+    assert np.array_equal(got, ref)
+    a = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, "fp16",
+                      kv_dtype="e4m3", k_scale=2.0, v_scale=3.0)
+    b = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale * 2.0, "fp16",
+                      kv_dtype="e4m3", k_scale=1.0, v_scale=1.0)
+    assert np.allclose(a, 3.0 * b, rtol=1e-13, atol=1e-14)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -34,6 +34,12 @@ MUTANTS = [
     ("first_token_dropped", "    for (int j = 0; j < n; ++j) {\n        double p", "    for (int j = 1; j < n; ++j) {\n        double p"),
     ("query_head", "const uint16_t *qrow = query + ((int64_t)i * Hq + h) * d;",
      "const uint16_t *qrow = query + ((int64_t)i * Hq + (h ^ 1) % Hq) * d;"),
+    ("e4m3_ties_up", "(frac == 0.5 && fmod(r, 2.0) == 1.0)", "(frac == 0.5)"),
+    ("e4m3_bias", "v = ldexp((double)(f + 8), e - 10);", "v = ldexp((double)(f + 8), e - 9);"),
+    ("e4m3_late_saturation", "if (a >= 448.0)", "if (a >= 480.0)"),
+    ("fp8_k_scale_dropped", "int rc = pa_oracle_gather(K, k_cache, kv_dtype, k_scale,",
+     "int rc = pa_oracle_gather(K, k_cache, kv_dtype, 1.0,"),
+    ("fp8_scatter_scale", "/ k_scale;", "* k_scale;"),
 ]
 
 RUNNER = r"""

@@ -57,6 +57,9 @@ class Workload:
     k_cache: torch.Tensor           # [NB, Hkv, bs, d] before the new token is written
     v_cache: torch.Tensor           # [NB, Hkv, bs, d]
     seed: int = 0
+    kv_dtype: str = ""              # "" = same as dtype; "e4m3": uint8 FP8 caches
+    k_scale: float = 1.0            # FP8 caches: code e stands for k_scale * e
+    v_scale: float = 1.0
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -68,7 +71,8 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2
+        """Bytes per cached K/V element."""
+        return 1 if self.kv_dtype == "e4m3" else 2
 
     def torch_dtype(self) -> torch.dtype:
         return DTYPES[self.dtype]
@@ -221,6 +225,29 @@ def _build(name, seed, dtype, B, Hq, Hkv, d, bs, ctx: np.ndarray, pool_slack: fl
 
 
 NAMES = ("tiny_mha", "llama3_8b_gqa", "shared_prefix_cow", "long_context", "llama3_70b_cb")
+
+FP8_POISON = 0x7F  # an E4M3 NaN code
+FP8_SCALE = float(np.float32(4.0 / 448.0))  # N(0,1) values up to 4 sigma fit the E4M3 range
+
+
+def to_fp8(w: Workload, k_scale: float = FP8_SCALE, v_scale: float = FP8_SCALE) -> Workload:
+    """The same workload with FP8 E4M3 caches: every owned slot holds the
+    nearest code (torch's float8_e4m3fn cast, after clamping to +-448) of its
+    N(0,1) value divided by the scale; unowned slots hold the NaN code.  The
+    query and the new token's K/V stay 16-bit (the scatter quantises them)."""
+    if w.dtype != "fp16":
+        raise ValueError("FP8 caches are paired with fp16 queries")
+    out = w.clone()
+
+    def quant(c, s):
+        x = (c.float() / s).clamp(-448.0, 448.0)
+        q = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        q[torch.isnan(c)] = FP8_POISON
+        return q
+    out.k_cache = quant(w.k_cache, k_scale)
+    out.v_cache = quant(w.v_cache, v_scale)
+    out.kv_dtype, out.k_scale, out.v_scale = "e4m3", float(k_scale), float(v_scale)
+    return out
 
 
 def make(name: str, seed: int = 0, *, dtype: Optional[str] = None, batch: Optional[int] = None,
