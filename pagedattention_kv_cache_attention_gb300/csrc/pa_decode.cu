@@ -73,7 +73,6 @@ template <int D, bool F8> struct Shape {
   static constexpr int kBoxes = kRowBytes / 128;         // boxes per row
   static constexpr int kBoxBytes = kTile * 128;          // one box of 16 rows
   static constexpr int kTileBytes = kTile * kRowBytes;   // K (or V) of one sub-tile
-  static constexpr int kStageBytes = 2 * kTileBytes;     // K + V
   static constexpr int kQChunks = D / 32;                // 16-byte q chunks per lane
   static constexpr int kMTiles = D / 16;                 // m16 tiles of the P.V product
 };
@@ -85,24 +84,29 @@ template <int D, bool F8> struct Shape {
 __device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
 
 // T: query/output type (and the MMA type); F8: the caches hold FP8 E4M3 codes
-// (T is then fp16), converted exactly to fp16 in registers.
-template <typename T, int D, int NW, int S, bool F8>
+// (T is then fp16), converted exactly to fp16 in registers.  NSUB: 16-token
+// sub-tiles per pipeline step (their MMA chains are independent and share one
+// softmax reduction).
+template <typename T, int D, int NW, int S, bool F8, int NSUB>
 __global__ void __launch_bounds__(NW * 32)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<D, F8>;
   static_assert(!F8 || (D == 128 && sizeof(T) == 2), "FP8 caches: head_dim 128, fp16 queries");
+  static_assert(NSUB == 1 || NSUB == 2, "one or two sub-tiles per step");
+  static_assert(S * NSUB <= 16, "stage bits");
+  constexpr int kStepBytes = 2 * NSUB * Sh::kTileBytes;  // K and V of one step
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled TMA destinations need 1024-byte alignment.
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * Sh::kStageBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * kStepBytes);
 
   const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
 
-  uint8_t *my_stages = smem + warp * S * Sh::kStageBytes;
+  uint8_t *my_stages = smem + warp * S * kStepBytes;
   uint64_t *my_bars = bars + warp * S;
   if (lane == 0) {
 #pragma unroll
@@ -114,15 +118,19 @@ __global__ void __launch_bounds__(NW * 32)
   // inputs (the pool above all) may come from the kernel launched just before
   grid_dependency_wait();
 
-  // Warp w takes sub-tiles w, w + NW, w + 2 NW, ... of the partition, so the
-  // block ids of its first 32 can be read before the context length arrives
-  // (entries past the sequence are read from the table row but never used).
+  // Step k of warp w covers sub-tiles (w + k NW) NSUB + h, h < NSUB, of the
+  // partition.  A "local" sub-tile index l = k NSUB + h numbers the warp's
+  // sub-tiles in order; lane l of a window holds the block id of local
+  // sub-tile (window base + l).  The first window is read before the context
+  // length arrives (entries past the sequence are read from the table row but
+  // never used).
   const int t_begin = part * a.part_tokens;
   const int full_sub = (a.part_tokens + kTile - 1) / kTile;
   const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
   const int bs_mask = (1 << a.bs_log2) - 1;
-  auto table_entry = [&](int k) -> int {
-    const int u = warp + k * NW;
+  auto sub_of = [&](int l) { return (warp + (l / NSUB) * NW) * NSUB + (l % NSUB); };
+  auto table_entry = [&](int l) -> int {
+    const int u = sub_of(l);
     if (u >= full_sub) return -1;
     const int lb = (t_begin + u * kTile) >> a.bs_log2;
     return lb < a.max_blocks_per_seq ? bt_row[lb] : -1;
@@ -137,50 +145,63 @@ __global__ void __launch_bounds__(NW * 32)
   if (part > 0 && t_begin >= ctx) return;  // partition past the end: nothing to write
   const int t_end = min(ctx, t_begin + a.part_tokens);
   const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
-  const int my_n = n_sub > warp ? (n_sub - warp + NW - 1) / NW : 0;  // this warp's sub-tiles
+  const int n_grp = (n_sub + NSUB - 1) / NSUB;
+  const int my_n = n_grp > warp ? (n_grp - warp + NW - 1) / NW : 0;  // this warp's steps
 
-  // physical block of the warp's k-th sub-tile, -1 if past its run or invalid
+  // physical block of local sub-tile l, -1 if past the partition or invalid
   // (an invalid entry is flagged and its tokens are masked)
-  auto checked = [&](int k, int phys) -> int {
-    if (k >= my_n) return -1;
+  auto checked = [&](int l, int phys) -> int {
+    if (l >= my_n * NSUB || sub_of(l) >= n_sub) return -1;
     if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
       atomicOr(a.err, kErrBadBlock);
       return -1;
     }
     return phys;
   };
-  auto tile_token = [&](int k) { return t_begin + (warp + k * NW) * kTile; };
+  auto sub_token = [&](int l) { return t_begin + sub_of(l) * kTile; };
 
   const uint64_t policy = l2_policy_evict_first();
-  // lane 0: start loading local sub-tile k into stage s
-  auto issue = [&](int k, int phys, int s) {
+  // lane 0: start loading the sub-tiles of step k into stage s
+  auto issue = [&](int k, const int (&phys)[NSUB], int s) {
     uint64_t *bar = &my_bars[s];
-    if (phys >= 0) {
-      mbar_arrive_expect_tx(bar, Sh::kStageBytes);
-      const int tok = tile_token(k);
-      const int y = ((phys * a.num_kv_heads + kvh) << a.bs_log2) + (tok & bs_mask);
-      uint8_t *st = my_stages + s * Sh::kStageBytes;
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) bytes += phys[h] >= 0 ? 2 * Sh::kTileBytes : 0;
+    if (bytes == 0) {
+      mbar_arrive(bar);  // nothing to load: complete the phase at once
+      return;
+    }
+    mbar_arrive_expect_tx(bar, bytes);
+    uint8_t *st = my_stages + s * kStepBytes;
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) {
+      if (phys[h] < 0) continue;
+      const int tok = sub_token(k * NSUB + h);
+      const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + (tok & bs_mask);
 #pragma unroll
       for (int b = 0; b < Sh::kBoxes; ++b) {
-        tma_load_2d(st + b * Sh::kBoxBytes, &kmap, b * Sh::kBoxElems, y, bar, policy);
-        tma_load_2d(st + Sh::kTileBytes + b * Sh::kBoxBytes, &vmap, b * Sh::kBoxElems, y, bar,
-                    policy);
+        tma_load_2d(st + h * Sh::kTileBytes + b * Sh::kBoxBytes, &kmap, b * Sh::kBoxElems, y,
+                    bar, policy);
+        tma_load_2d(st + (NSUB + h) * Sh::kTileBytes + b * Sh::kBoxBytes, &vmap,
+                    b * Sh::kBoxElems, y, bar, policy);
       }
-    } else {
-      mbar_arrive(bar);  // nothing to load: complete the phase at once
     }
   };
 
-  // block ids of the warp's sub-tiles [win_base, win_base + 32) and the next 32
+  // block ids of the warp's local sub-tiles [win_base, win_base + 32) and the next 32
   int win_base = 0;
   win = checked(lane, win);
-  int win_next = my_n > 32 ? checked(32 + lane, table_entry(32 + lane)) : -1;
-  uint32_t stage_ok = 0;  // bit s: the sub-tile in stage s has a valid block
+  int win_next = my_n * NSUB > 32 ? checked(32 + lane, table_entry(32 + lane)) : -1;
+  uint32_t stage_ok = 0;  // bit s NSUB + h: sub-tile h of the step in stage s is valid
 #pragma unroll
   for (int s = 0; s < S; ++s) {
     if (s < my_n) {
-      const int phys = __shfl_sync(kFull, win, s);
-      stage_ok |= (phys >= 0 ? 1u : 0u) << s;
+      int phys[NSUB];
+#pragma unroll
+      for (int h = 0; h < NSUB; ++h) {
+        phys[h] = __shfl_sync(kFull, win, s * NSUB + h);
+        stage_ok |= (phys[h] >= 0 ? 1u : 0u) << (s * NSUB + h);
+      }
       if (lane == 0) issue(s, phys, s);
     }
   }
@@ -218,50 +239,64 @@ __global__ void __launch_bounds__(NW * 32)
       k_stop = k;
       break;
     }
-    const bool ok = (stage_ok >> s) & 1u;
-    const int tok0 = tile_token(k);
-    const int nvalid = ok ? min(kTile, t_end - tok0) : 0;
-    const uint8_t *Ks = my_stages + s * Sh::kStageBytes;
-    const uint8_t *Vs = Ks + Sh::kTileBytes;
+    const uint8_t *stage = my_stages + s * kStepBytes;
+    int nvalid[NSUB];
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) {
+      const bool ok = (stage_ok >> (s * NSUB + h)) & 1u;
+      nvalid[h] = ok ? max(0, min(kTile, t_end - sub_token(k * NSUB + h))) : 0;
+    }
 
-    // ---- S^T = K Q^T : rows g and g+8 (tokens), columns 2c, 2c+1 (heads)
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!F8) {
+    // ---- S^T = K Q^T per sub-tile: rows g and g+8 (tokens), columns 2c, 2c+1 (heads)
+    float sc[NSUB][4];
 #pragma unroll
-      for (int i = 0; i < Sh::kQChunks; ++i) {
-        const int ch = q_chunk(i, c);
-        const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
-        const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
-        const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
-        const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
-        Elem<T>::mma(sc, ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
-        Elem<T>::mma(sc, ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
-      }
-    } else {
-      // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
+    for (int h = 0; h < NSUB; ++h) {
+      const uint8_t *Ks = stage + h * Sh::kTileBytes;
+      sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
+      if constexpr (!F8) {
 #pragma unroll
-      for (int j = 0; j < D / 64; ++j) {
-        const int sw = ((2 * c + j) ^ g) << 4;
-        uint32_t ka[8], kb[8];
-        e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + g * 128 + sw), ka);
-        e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + (g + 8) * 128 + sw), kb);
-        const uint32_t q[8] = {qf[2 * j].x, qf[2 * j].y, qf[2 * j].z, qf[2 * j].w,
-                               qf[2 * j + 1].x, qf[2 * j + 1].y, qf[2 * j + 1].z,
-                               qf[2 * j + 1].w};
+        for (int i = 0; i < Sh::kQChunks; ++i) {
+          const int ch = q_chunk(i, c);
+          const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
+          const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
+          const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
+          const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
+          Elem<T>::mma(sc[h], ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
+          Elem<T>::mma(sc[h], ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
+        }
+      } else {
+        // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          Elem<T>::mma(sc, ka[2 * t], kb[2 * t], ka[2 * t + 1], kb[2 * t + 1], q[2 * t],
-                       q[2 * t + 1]);
+        for (int j = 0; j < D / 64; ++j) {
+          const int sw = ((2 * c + j) ^ g) << 4;
+          uint32_t ka[8], kb[8];
+          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + g * 128 + sw), ka);
+          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + (g + 8) * 128 + sw), kb);
+          const uint32_t q[8] = {qf[2 * j].x, qf[2 * j].y, qf[2 * j].z, qf[2 * j].w,
+                                 qf[2 * j + 1].x, qf[2 * j + 1].y, qf[2 * j + 1].z,
+                                 qf[2 * j + 1].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            Elem<T>::mma(sc[h], ka[2 * t], kb[2 * t], ka[2 * t + 1], kb[2 * t + 1], q[2 * t],
+                         q[2 * t + 1]);
+        }
       }
     }
 
-    // ---- online softmax in base 2 (log2(e) folded into the scale)
-    const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
-    const float x0 = v_lo ? sc[0] * a.scale_log2 : NEG_INF;
-    const float x1 = v_lo ? sc[1] * a.scale_log2 : NEG_INF;
-    const float x2 = v_hi ? sc[2] * a.scale_log2 : NEG_INF;
-    const float x3 = v_hi ? sc[3] * a.scale_log2 : NEG_INF;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    // ---- online softmax in base 2 (log2(e) folded into the scale), one
+    // reduction over all NSUB x 16 tokens of the step
+    float x[NSUB][4];
+    float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) {
+      const bool v_lo = g < nvalid[h], v_hi = g + 8 < nvalid[h];
+      x[h][0] = v_lo ? sc[h][0] * a.scale_log2 : NEG_INF;
+      x[h][1] = v_lo ? sc[h][1] * a.scale_log2 : NEG_INF;
+      x[h][2] = v_hi ? sc[h][2] * a.scale_log2 : NEG_INF;
+      x[h][3] = v_hi ? sc[h][3] * a.scale_log2 : NEG_INF;
+      mx0 = fmaxf(mx0, fmaxf(x[h][0], x[h][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[h][1], x[h][3]));
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
@@ -271,10 +306,19 @@ __global__ void __launch_bounds__(NW * 32)
     const float r0 = mn0 == NEG_INF ? 0.f : mn0;  // no valid token yet: any finite reference
     const float r1 = mn1 == NEG_INF ? 0.f : mn1;
     const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
-    const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1);
-    const float p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
+    float p[NSUB][4];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int h = 0; h < NSUB; ++h) {
+      p[h][0] = exp2f(x[h][0] - r0);
+      p[h][1] = exp2f(x[h][1] - r1);
+      p[h][2] = exp2f(x[h][2] - r0);
+      p[h][3] = exp2f(x[h][3] - r1);
+      ps0 += p[h][0] + p[h][2];
+      ps1 += p[h][1] + p[h][3];
+    }
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
     m0 = mn0;
     m1 = mn1;
     if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
@@ -286,77 +330,88 @@ __global__ void __launch_bounds__(NW * 32)
         acc[mt][3] *= al1;
       }
     }
-    // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g).  P is
-    // carried as hi + lo in the KV dtype (hi = P rounded, lo = the exact fp32
-    // remainder rounded), so the P.V product keeps ~16 (bf16) or ~22 (fp16)
-    // bits of P instead of 8 or 11.
-    const uint32_t h01 = Elem<T>::pack(p0, p1), h23 = Elem<T>::pack(p2, p3);
-    const float2 f01 = Elem<T>::unpack(h01), f23 = Elem<T>::unpack(h23);
-    const uint32_t pb0 = movmatrix_trans(h01);
-    const uint32_t pb1 = movmatrix_trans(h23);
-    const uint32_t pr0 = movmatrix_trans(Elem<T>::pack(p0 - f01.x, p1 - f01.y));
-    const uint32_t pr1 = movmatrix_trans(Elem<T>::pack(p2 - f23.x, p3 - f23.y));
 
-    // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; unit g of every box
-    if constexpr (!F8) {
-      uint4 v[4][Sh::kBoxes];
 #pragma unroll
-      for (int ri = 0; ri < 4; ++ri) {
-        const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
-        const bool keep = r < nvalid;
+    for (int h = 0; h < NSUB; ++h) {
+      // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g).  P is
+      // carried as hi + lo in the MMA type (hi = P rounded, lo = the exact fp32
+      // remainder rounded), so the P.V product keeps ~16 (bf16) or ~22 (fp16)
+      // bits of P instead of 8 or 11.
+      const uint32_t h01 = Elem<T>::pack(p[h][0], p[h][1]);
+      const uint32_t h23 = Elem<T>::pack(p[h][2], p[h][3]);
+      const float2 f01 = Elem<T>::unpack(h01), f23 = Elem<T>::unpack(h23);
+      const uint32_t pb0 = movmatrix_trans(h01);
+      const uint32_t pb1 = movmatrix_trans(h23);
+      const uint32_t pr0 = movmatrix_trans(Elem<T>::pack(p[h][0] - f01.x, p[h][1] - f01.y));
+      const uint32_t pr1 = movmatrix_trans(Elem<T>::pack(p[h][2] - f23.x, p[h][3] - f23.y));
+      const uint8_t *Vs = stage + (NSUB + h) * Sh::kTileBytes;
+
+      // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; unit g of every box
+      if constexpr (!F8) {
+        uint4 v[4][Sh::kBoxes];
 #pragma unroll
-        for (int b = 0; b < Sh::kBoxes; ++b) {
-          const uint4 x = *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 +
-                                                           ((g ^ (r & 7)) << 4));
-          v[ri][b] = keep ? x : make_uint4(0, 0, 0, 0);
+        for (int ri = 0; ri < 4; ++ri) {
+          const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
+          const bool keep = r < nvalid[h];
+#pragma unroll
+          for (int b = 0; b < Sh::kBoxes; ++b) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 +
+                                                              ((g ^ (r & 7)) << 4));
+            v[ri][b] = keep ? xv : make_uint4(0, 0, 0, 0);
+          }
         }
-      }
 #pragma unroll
-      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-        // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
-        constexpr int bA = 0;
-        constexpr int bB = Sh::kBoxes - 1;
-        const int eA = mt;
-        const int eB = D == 128 ? mt : 4 + mt;
-        const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
-        const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
-        const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
-        const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
-        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
-      }
-    } else {
-      // unit g (dims 16g .. 16g+15) of each row, converted to fp16
-      uint32_t vh[4][8];
+        for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+          // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
+          constexpr int bA = 0;
+          constexpr int bB = Sh::kBoxes - 1;
+          const int eA = mt;
+          const int eB = D == 128 ? mt : 4 + mt;
+          const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
+          const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
+          const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
+          const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
+          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+        }
+      } else {
+        // unit g (dims 16g .. 16g+15) of each row, converted to fp16
+        uint32_t vh[4][8];
 #pragma unroll
-      for (int ri = 0; ri < 4; ++ri) {
-        const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
-        const uint4 x = *reinterpret_cast<const uint4 *>(Vs + r * 128 + ((g ^ (r & 7)) << 4));
-        e4m3x16_to_half(r < nvalid ? x : make_uint4(0, 0, 0, 0), vh[ri]);
-      }
+        for (int ri = 0; ri < 4; ++ri) {
+          const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
+          const uint4 xv = *reinterpret_cast<const uint4 *>(Vs + r * 128 + ((g ^ (r & 7)) << 4));
+          e4m3x16_to_half(r < nvalid[h] ? xv : make_uint4(0, 0, 0, 0), vh[ri]);
+        }
 #pragma unroll
-      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-        // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt
-        const uint32_t a0 = pair_of16(vh[0], vh[1], mt);
-        const uint32_t a1 = pair_of16(vh[0], vh[1], 8 + mt);
-        const uint32_t a2 = pair_of16(vh[2], vh[3], mt);
-        const uint32_t a3 = pair_of16(vh[2], vh[3], 8 + mt);
-        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-        Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+        for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+          // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt
+          const uint32_t a0 = pair_of16(vh[0], vh[1], mt);
+          const uint32_t a1 = pair_of16(vh[0], vh[1], 8 + mt);
+          const uint32_t a2 = pair_of16(vh[2], vh[3], mt);
+          const uint32_t a3 = pair_of16(vh[2], vh[3], 8 + mt);
+          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+        }
       }
     }
 
-    // ---- refill this stage with local sub-tile k + S
+    // ---- refill this stage with step k + S
     __syncwarp();
     const int nk = k + S;
     if (nk < my_n) {
-      if (nk >= win_base + 32) {
+      if (nk * NSUB >= win_base + 32) {
         win_base += 32;
         win = win_next;
         win_next = checked(win_base + 32 + lane, table_entry(win_base + 32 + lane));
       }
-      const int phys = __shfl_sync(kFull, win, nk - win_base);
-      stage_ok = (stage_ok & ~(1u << s)) | ((phys >= 0 ? 1u : 0u) << s);
+      int phys[NSUB];
+#pragma unroll
+      for (int h = 0; h < NSUB; ++h) {
+        phys[h] = __shfl_sync(kFull, win, nk * NSUB + h - win_base);
+        stage_ok = (stage_ok & ~(1u << (s * NSUB + h))) |
+                   ((phys[h] >= 0 ? 1u : 0u) << (s * NSUB + h));
+      }
       if (lane == 0) {
         fence_proxy_async_smem();
         issue(nk, phys, s);
@@ -553,15 +608,16 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_
   return r == CUDA_SUCCESS;
 }
 
-template <typename T, int D, int NW, int S, bool F8>
+template <typename T, int D, int NW, int S, bool F8, int NSUB>
 cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                             cudaStream_t stream) {
   using Sh = Shape<D, F8>;
-  constexpr size_t smem = 1024 + static_cast<size_t>(NW) * S * Sh::kStageBytes + NW * S * 8;
+  constexpr size_t step = 2 * NSUB * Sh::kTileBytes;
+  constexpr size_t smem = 1024 + static_cast<size_t>(NW) * S * step + NW * S * 8;
   static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 <=
-                    static_cast<size_t>(NW) * S * Sh::kStageBytes,
+                    static_cast<size_t>(NW) * S * step,
                 "merge buffers must fit in the stage area");
-  auto kern = pa_decode_kernel<T, D, NW, S, F8>;
+  auto kern = pa_decode_kernel<T, D, NW, S, F8, NSUB>;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -597,9 +653,21 @@ cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
 constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStages = PA_DECODE_STAGES;
 
-// FP8 caches have half the bytes per stage: twice the stages keep as many
-// bytes in flight per warp.
-constexpr int kStagesF8 = 2 * kStages;
+// Sub-tiles per pipeline step.  FP8 tiles carry half the bytes, so two of
+// them per step keep the bytes per step, and the per-step latency chain is
+// shared by twice the tokens.
+#ifndef PA_DECODE_NSUB
+#define PA_DECODE_NSUB 1
+#endif
+#ifndef PA_DECODE_NSUB_F8
+#define PA_DECODE_NSUB_F8 2
+#endif
+#ifndef PA_DECODE_STAGES_F8
+#define PA_DECODE_STAGES_F8 2
+#endif
+constexpr int kNsub = PA_DECODE_NSUB;
+constexpr int kNsubF8 = PA_DECODE_NSUB_F8;
+constexpr int kStagesF8 = PA_DECODE_STAGES_F8;
 
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
@@ -611,15 +679,18 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
     *map_failed = true;
     return cudaErrorInvalidValue;
   }
-  if (kv_fp8) return launch_decode_t<__half, 128, kWarps, kStagesF8, true>(a, km, vm, stream);
+  if (kv_fp8)
+    return launch_decode_t<__half, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream);
   if (dtype == 0) {
     return head_dim == 128
-               ? launch_decode_t<__half, 128, kWarps, kStages, false>(a, km, vm, stream)
-               : launch_decode_t<__half, 64, kWarps, kStages, false>(a, km, vm, stream);
+               ? launch_decode_t<__half, 128, kWarps, kStages, false, kNsub>(a, km, vm, stream)
+               : launch_decode_t<__half, 64, kWarps, kStages, false, kNsub>(a, km, vm, stream);
   }
   return head_dim == 128
-             ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages, false>(a, km, vm, stream)
-             : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages, false>(a, km, vm, stream);
+             ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages, false, kNsub>(a, km, vm,
+                                                                                   stream)
+             : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages, false, kNsub>(a, km, vm,
+                                                                                 stream);
 }
 
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream) {
