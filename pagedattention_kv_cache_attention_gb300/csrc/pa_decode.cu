@@ -375,23 +375,34 @@ __global__ void __launch_bounds__(NW * 32)
           Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
         }
       } else {
-        // unit g (dims 16g .. 16g+15) of each row, converted to fp16
-        uint32_t vh[4][8];
+        // unit g (dims 16g .. 16g+15) of each row, still E4M3
+        uint4 v8[4];
 #pragma unroll
         for (int ri = 0; ri < 4; ++ri) {
           const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
           const uint4 xv = *reinterpret_cast<const uint4 *>(Vs + r * 128 + ((g ^ (r & 7)) << 4));
-          e4m3x16_to_half(r < nvalid[h] ? xv : make_uint4(0, 0, 0, 0), vh[ri]);
+          v8[ri] = r < nvalid[h] ? xv : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-          // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt
-          const uint32_t a0 = pair_of16(vh[0], vh[1], mt);
-          const uint32_t a1 = pair_of16(vh[0], vh[1], 8 + mt);
-          const uint32_t a2 = pair_of16(vh[2], vh[3], mt);
-          const uint32_t a3 = pair_of16(vh[2], vh[3], 8 + mt);
-          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+        for (int mt = 0; mt < Sh::kMTiles; mt += 2) {
+          // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt; each byte
+          // interleave yields the (token 2c, token 2c+1) pairs of two m-tiles
+          const uint32_t w0 = interleave_bytes(v8[0], v8[1], mt);
+          const uint32_t w1 = interleave_bytes(v8[0], v8[1], 8 + mt);
+          const uint32_t w2 = interleave_bytes(v8[2], v8[3], mt);
+          const uint32_t w3 = interleave_bytes(v8[2], v8[3], 8 + mt);
+          {
+            const uint32_t a0 = e4m3x2_lo_to_f16x2(w0), a1 = e4m3x2_lo_to_f16x2(w1);
+            const uint32_t a2 = e4m3x2_lo_to_f16x2(w2), a3 = e4m3x2_lo_to_f16x2(w3);
+            Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+          }
+          {
+            const uint32_t a0 = e4m3x2_hi_to_f16x2(w0), a1 = e4m3x2_hi_to_f16x2(w1);
+            const uint32_t a2 = e4m3x2_hi_to_f16x2(w2), a3 = e4m3x2_hi_to_f16x2(w3);
+            Elem<T>::mma(acc[mt + 1], a0, a1, a2, a3, pb0, pb1);
+            Elem<T>::mma(acc[mt + 1], a0, a1, a2, a3, pr0, pr1);
+          }
         }
       }
     }

@@ -167,25 +167,41 @@ __device__ __forceinline__ uint32_t pair_of(const uint4 &x, const uint4 &y, int 
   return __byte_perm(word_of(x, e >> 1), word_of(y, e >> 1), (e & 1) ? 0x7632 : 0x5410);
 }
 
-// 16 FP8 E4M3 values (one 16-byte load, element 0 in the lowest byte) to 8
-// words of fp16 pairs in the same order.  Every E4M3 value is exact in fp16.
+// Two FP8 E4M3 values (bits 0-7 and 8-15, or 16-23 and 24-31, of w) to an
+// fp16 pair in one register, first value in the low half.  Every E4M3 value is
+// exact in fp16.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+      : "=r"(d)
+      : "r"(w));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
+      : "=r"(d)
+      : "r"(w));
+  return d;
+}
+
+// 16 E4M3 values (one 16-byte load, element 0 in the lowest byte) to 8 words
+// of fp16 pairs in the same order.
 __device__ __forceinline__ void e4m3x16_to_half(const uint4 &x, uint32_t (&h)[8]) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-    h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-    h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+    h[2 * i] = e4m3x2_lo_to_f16x2(w[i]);
+    h[2 * i + 1] = e4m3x2_hi_to_f16x2(w[i]);
   }
 }
 
-// Elements e of two 16-element fp16 rows (8 words each): x's in the low half.
-__device__ __forceinline__ uint32_t pair_of16(const uint32_t (&x)[8], const uint32_t (&y)[8],
-                                              int e) {
-  return __byte_perm(x[e >> 1], y[e >> 1], (e & 1) ? 0x7632 : 0x5410);
+// Bytes e and e+1 (e even, < 16) of two 16-byte rows x and y interleaved as
+// (x_e, y_e, x_e+1, y_e+1): two (x, y) pairs ready for e4m3x2_*_to_f16x2.
+__device__ __forceinline__ uint32_t interleave_bytes(const uint4 &x, const uint4 &y, int e) {
+  const int b = e & 3;  // 0 or 2
+  return __byte_perm(word_of(x, e >> 2), word_of(y, e >> 2),
+                     b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12));
 }
 
 }  // namespace pa
