@@ -546,6 +546,55 @@ def run_block_ops(args):
     return 0
 
 
+def prefill_flops(pw) -> int:
+    """Useful FLOPs of causal chunked prefill: each (row, query head) attends to
+    pos + 1 keys at 4 d FLOPs per key (QK^T and P.V)."""
+    import numpy as np
+    ctx = pw.context_lens.numpy().astype(np.int64)
+    ql = pw.q_lens.numpy().astype(np.int64)
+    # sum over t < q of (ctx - q + t + 1) = q (ctx - q + 1) + q (q - 1) / 2
+    keys = (ql * (ctx - ql + 1) + ql * (ql - 1) // 2).sum()
+    return int(4 * pw.head_dim * pw.num_q_heads * keys)
+
+
+def run_prefill(args):
+    """Chunked-prefill throughput: scatter of the chunk tokens then pa_prefill."""
+    import torch
+
+    import pagedattention_kv_cache_attention_gb300 as pa
+    import workloads
+    dev = torch.device("cuda", 0)
+    kw = dict(dtype=args.dtype) if args.dtype else {}
+    pw = workloads.make_prefill(args.workload, seed=args.seed, chunk=args.chunk, **kw)
+    kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
+    key, value, sm = pw.key.to(dev), pw.value.to(dev), pw.slot_mapping.to(dev)
+    q, qs = pw.query.to(dev), pw.query_start.to(dev)
+    bt, cl = pw.block_tables.to(dev), pw.context_lens.to(dev)
+    out = torch.empty_like(q)
+    pa.pa_reshape_and_cache(key, value, kc, vc, sm)
+
+    def call():
+        pa.pa_prefill(out, q, qs, kc, vc, bt, cl, pw.scale, pw.max_q_len)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    if pa.pa_device_errors() != 0:
+        raise RuntimeError("device error bits raised")
+    fl = prefill_flops(pw)
+    print(json.dumps({"op": "prefill", "workload": pw.name, "chunk": args.chunk,
+                      "seqs": pw.num_seqs, "total_q": pw.total_q, "dtype": pw.dtype,
+                      "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                      "tokens_per_s": round(pw.total_q / (ms * 1e-3), 1)}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -562,14 +611,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of host time for the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("step", "blocks"), default="step",
-                    help="step: the decode step (default); blocks: copy/swap block bandwidth")
+    ap.add_argument("--op", choices=("step", "blocks", "prefill"), default="step",
+                    help="step: the decode step (default); blocks: copy/swap block bandwidth; "
+                         "prefill: chunked-prefill attention")
+    ap.add_argument("--chunk", type=int, default=512, help="prefill chunk (tokens)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "blocks":
         return run_block_ops(args)
+    if args.op == "prefill":
+        return run_prefill(args)
     return run_ours(args)
 
 

@@ -169,6 +169,35 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
                            int32_t dtype, void *stream);
 
 /*
+ * pa_prefill -- chunked-prefill attention over the paged cache ("Serving
+ * engines", How vLLM works: chunked prefill slices a long prompt into pieces;
+ * "LLM Serving Engine Shootout", 1: prefill attends over all prompt tokens).
+ *
+ * Sequence i appends q_len_i = query_start[i+1] - query_start[i] tokens, query
+ * rows query_start[i] .. query_start[i+1]-1, whose K/V are already in the
+ * cache (pa_reshape_and_cache of those tokens), so the sequence now holds
+ * context_lens[i] >= q_len_i tokens.  Chunk row t sits at position
+ * p = context_lens[i] - q_len_i + t and attends causally:
+ *   out[row, h, :] = sum_{j <= p} softmax_j(scale q[row, h] . K_j) V_j
+ * with K_j, V_j read through the block table as in pa_decode.
+ *
+ * query, out     device, [total_q, num_q_heads, head_dim], dtype; 16-byte aligned
+ * query_start    device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
+ * max_q_len      >= every q_len_i (sizes the launch)
+ * Softmax and accumulation fp32; out rounded to dtype.  head_dim in {64, 128},
+ * block_size in {16, 32}, num_q_heads / num_kv_heads in 1..8.  A q_len_i
+ * larger than context_lens[i] or than max_q_len, or a context longer than the
+ * table, skips that sequence and sets PA_DEVERR_BAD_LEN.
+ */
+pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
+                     const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                     const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t block_size, int64_t num_blocks, float scale,
+                     int32_t dtype, void *stream);
+
+/*
  * FP8 KV cache.  The cache stores one byte per element, an FP8 E4M3 code
  * (1 sign, 4 exponent bits with bias 7, 3 fraction bits, no infinities,
  * largest magnitude 448), with one scale per cache: code e stands for

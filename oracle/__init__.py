@@ -69,6 +69,9 @@ def _load(path: str) -> ctypes.CDLL:
     L.pa_oracle_lse_combine.argtypes = [P, P, P, P, P, i32, i32, i32]
     L.pa_oracle_lse_combine.restype = None
     L.pa_oracle_max_threads.restype = i32
+    L.pa_oracle_prefill.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64,
+                                    ctypes.c_float, i32, i32]
+    L.pa_oracle_prefill.restype = i32
     return L
 
 
@@ -190,6 +193,28 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, scale: float, dt
         out = out.reshape(B, Hq, d)
     if return_partials:
         return out, pm, pl, po
+    return out
+
+
+def prefill(query, query_start, k_cache, v_cache, block_tables, context_lens, scale: float,
+            dtype: str, threads: int = 0) -> np.ndarray:
+    """fp64 causal attention of each chunk row (position ctx - q_len + t) over
+    tokens 0 .. its position.  query [total_q, Hq, d]; returns the same shape."""
+    q = _u16(query)
+    qs = _i32(query_start)
+    kc = _u16(k_cache)
+    vc = _u16(v_cache)
+    bt = _i32(block_tables)
+    cl = _i32(context_lens)
+    total_q, Hq, d = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    B = cl.shape[0]
+    assert qs.shape[0] == B + 1 and int(qs[-1]) == total_q
+    out = np.empty((total_q, Hq, d), dtype=np.float64)
+    rc = lib().pa_oracle_prefill(_p(out), _p(q), _p(qs), _p(kc), _p(vc), _p(bt), bt.shape[1],
+                                 _p(cl), B, Hq, Hkv, d, bs, NB, float(scale), DT[dtype], threads)
+    if rc:
+        raise IndexError(f"oracle prefill: status {rc}")
     return out
 
 

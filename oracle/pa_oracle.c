@@ -403,6 +403,78 @@ int pa_oracle_decode(double *out, double *part_m, double *part_l, double *part_o
 }
 
 /*
+ * Prefill (chunked-prefill) attention over the paged cache ("Serving engines",
+ * How vLLM works: chunked prefill slices a prompt into pieces; "LLM Serving
+ * Engine Shootout", 1: prefill attends over all prompt tokens).  The chunk of
+ * sequence i is query rows query_start[i] .. query_start[i+1]-1 (q_len_i
+ * rows); its K/V are already in the cache, whose sequence now holds ctx_i =
+ * context_lens[i] tokens.  Row t of the chunk sits at position
+ * p = ctx_i - q_len_i + t and attends causally to tokens 0 .. p:
+ *   out[row, h, :] = softmax_j(scale q[row, h] . K_j) V_j over j <= p.
+ * query/out [total_q, Hq, d].  Rows are independent; each is the decode
+ * computation on the sequence cut after position p.
+ */
+int pa_oracle_prefill(double *out, const uint16_t *query, const int32_t *query_start,
+                      const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                      int MB, const int32_t *context_lens, int B, int Hq, int Hkv, int d, int bs,
+                      int64_t NB, float scale, int dtype, int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || bs <= 0)
+        return ORC_BAD_ARG;
+    int total_q = B > 0 ? query_start[B] : 0;
+    int group = Hq / Hkv;
+    double sc = (double)scale;
+    int status = ORC_OK;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int k = 0; k < total_q * Hq; ++k) {
+        int row = k / Hq, h = k % Hq;
+        int i = 0;
+        while (i < B && query_start[i + 1] <= row)
+            ++i;
+        int q_len = query_start[i + 1] - query_start[i];
+        int ctx = context_lens[i];
+        int pos = ctx - q_len + (row - query_start[i]);
+        double *o = out + (int64_t)k * d;
+        if (pos < 0 || pos >= ctx) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORC_BAD_ARG;
+            continue;
+        }
+        int n = pos + 1;
+        double *K = malloc(sizeof(double) * ((size_t)n * d + 1));
+        double *V = malloc(sizeof(double) * ((size_t)n * d + 1));
+        double *q = malloc(sizeof(double) * (size_t)d);
+        double *s = malloc(sizeof(double) * ((size_t)n + 1));
+        int rc = (K && V && q && s) ? ORC_OK : ORC_NO_MEM;
+        const int32_t *bt_row = block_tables + (int64_t)i * MB;
+        if (rc == ORC_OK)
+            rc = pa_oracle_gather(K, k_cache, dtype, 1.0, bt_row, MB, n, Hkv, h / group, d, bs, NB);
+        if (rc == ORC_OK)
+            rc = pa_oracle_gather(V, v_cache, dtype, 1.0, bt_row, MB, n, Hkv, h / group, d, bs, NB);
+        if (rc == ORC_OK) {
+            const uint16_t *qrow = query + ((int64_t)row * Hq + h) * d;
+            for (int c = 0; c < d; ++c)
+                q[c] = to_f64(qrow[c], dtype);
+            double m, l;
+            attend(o, &m, &l, q, K, V, n, d, sc, s);
+        } else {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = rc;
+        }
+        free(K); free(V); free(q); free(s);
+    }
+    return status;
+}
+
+/*
  * Join partition results by log-sum-exp, the combination step stated above,
  * for inputs that did not come from pa_oracle_decode (for example fp32
  * partials rounded from it).  m, l: [n, P]; o: [n, P, d]; nparts[k] partitions

@@ -24,7 +24,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
     "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
     "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
-    "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -341,6 +341,38 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
         block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, d,
         bs, NB, float(scale), float(k_scale), float(v_scale), int(max_context_len),
         int(partition_size), ws_ptr or None, ws_bytes, _dtype_code(query), _stream(stream)))
+    return out
+
+
+def pa_prefill(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor,
+               k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, scale: float, max_q_len: int,
+               stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention into ``out`` [total_q, Hq, d]: row t of
+    sequence i's chunk (rows query_start[i]..query_start[i+1]-1) sits at
+    position context_lens[i] - q_len_i + t and attends to tokens 0..that."""
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f = _blocks_fn("pa_prefill", [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
+                                  f32, i32, P])
+    dt = k_cache.dtype
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, dt)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for n, t in (("query_start", query_start), ("block_tables", block_tables),
+                 ("context_lens", context_lens)):
+        _cuda(n, t, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    total_q, Hq, d = query.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    B = context_lens.numel()
+    if query_start.numel() != B + 1 or out.shape != query.shape:
+        raise ValueError("query_start must have num_seqs + 1 entries; out must match query")
+    _check("pa_prefill", f(out.data_ptr(), query.data_ptr(), query_start.data_ptr(),
+                           k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+                           block_tables.shape[1], context_lens.data_ptr(), B, int(max_q_len), Hq,
+                           Hkv, d, bs, NB, float(scale), _dtype_code(k_cache), _stream(stream)))
     return out
 
 

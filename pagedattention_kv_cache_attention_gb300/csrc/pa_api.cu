@@ -315,6 +315,52 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t k
                                                                                   : PA_ERR_CUDA;
 }
 
+pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
+                     const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                     int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
+                     int32_t dtype, void *stream) {
+  if (num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0 || !dtype_ok(dtype) || !std::isfinite(scale))
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size) || group > 8)
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (!out || !query || !query_start || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const int64_t pool_rows = num_blocks * num_kv_heads * block_size;
+  if (pool_rows >= (int64_t(1) << 31) || num_seqs > 65535 || num_kv_heads > 65535)
+    return PA_ERR_UNSUPPORTED;
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
+  pa::PrefillArgs a;
+  a.out = out;
+  a.query = query;
+  a.query_start = query_start;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  a.bs_log2 = block_size == 16 ? 4 : 5;
+  a.max_q_len = max_q_len;
+  a.num_blocks = num_blocks;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = err;
+  bool map_failed = false;
+  if (pa::launch_prefill(a, k_cache, v_cache, pool_rows, head_dim, dtype,
+                         static_cast<cudaStream_t>(stream), &map_failed) != cudaSuccess)
+    return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
+  return PA_OK;
+}
+
 pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                          int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, int64_t num_blocks, void *stream) {

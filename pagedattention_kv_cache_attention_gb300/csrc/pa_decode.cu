@@ -599,6 +599,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // The pool viewed as a 2-D tensor [num_blocks * num_kv_heads * block_size rows,
 // head_dim] loaded in boxes of 16 rows x 128 bytes with the 128-byte swizzle.
 bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
@@ -618,6 +620,8 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <typename T, int D, int NW, int S, bool F8, int NSUB>
 cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,

@@ -48,6 +48,19 @@ struct ReshapeArgs {
   unsigned *err;
 };
 
+struct PrefillArgs {
+  void *out;                    // [total_q, Hq, D]
+  const void *query;            // [total_q, Hq, D]
+  const int32_t *query_start;   // [B + 1]
+  const int32_t *block_tables;  // [B, max_blocks_per_seq]
+  const int32_t *context_lens;  // [B], the chunk included
+  int max_blocks_per_seq;
+  int num_seqs, num_q_heads, num_kv_heads, group, bs_log2, max_q_len;
+  int64_t num_blocks;
+  float scale_log2;
+  unsigned *err;
+};
+
 struct BlockCopyArgs {
   const void *src[2];           // per tensor: source pool (device or mapped host memory)
   void *dst[2];                 // per tensor: destination pool
@@ -84,5 +97,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
 cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,
+                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                           bool *map_failed);
 
 }  // namespace pa

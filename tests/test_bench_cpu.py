@@ -43,3 +43,10 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["metric"] == bench.METRIC
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_prefill_flops_by_hand():
+    pw = W.make_prefill("tiny_mha", 0, lens=[10, 4], q_lens=[3, 4])
+    # seq 0: positions 7, 8, 9 -> 8 + 9 + 10 keys; seq 1: positions 0..3 -> 1+2+3+4 keys
+    keys = (8 + 9 + 10) + (1 + 2 + 3 + 4)
+    assert bench.prefill_flops(pw) == 4 * 64 * 4 * keys

@@ -1,0 +1,99 @@
+"""The decode step captured in a CUDA graph ("Inference Engines": CUDA graphs
+cut launch overhead).  Every library call only validates on the host and
+enqueues kernels, so a captured step replayed with new inputs written into the
+captured buffers must give the bit-identical result of the same calls made
+eagerly."""
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from pagedattention_kv_cache_attention_gb300 import build
+    build.build()
+    import pagedattention_kv_cache_attention_gb300 as pa
+    pa._load()
+    assert pa.pa_device_errors() == 0
+    return pa
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_captured_step_replays_bitwise(pa, fp8):
+    base = W.make("llama3_8b_gqa", 51, batch=16)
+    other = W.make("llama3_8b_gqa", 52, batch=16)   # same shapes, new values and lengths
+    if fp8:
+        base, other = W.to_fp8(base), W.to_fp8(other)
+    dev = torch.device("cuda")
+    maxctx = max(base.max_context_len, other.max_context_len)
+    NB = max(base.num_blocks, other.num_blocks)
+    ps = 512
+
+    def buffers(w):
+        kc = torch.zeros((NB,) + tuple(w.k_cache.shape[1:]), dtype=w.k_cache.dtype, device=dev)
+        vc = torch.zeros_like(kc)
+        kc[:w.num_blocks] = w.k_cache.to(dev)
+        vc[:w.num_blocks] = w.v_cache.to(dev)
+        return dict(kc=kc, vc=vc, key=w.key.to(dev), value=w.value.to(dev),
+                    sm=w.slot_mapping.to(dev), q=w.query.to(dev), bt=w.block_tables.to(dev),
+                    cl=w.context_lens.to(dev), out=torch.empty_like(w.query, device=dev))
+
+    ws = torch.empty(pa.pa_decode_workspace_size(base.num_seqs, base.num_q_heads,
+                                                 base.head_dim, maxctx, ps),
+                     dtype=torch.uint8, device=dev)
+
+    def step(b, w, stream=None):
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(b["key"], b["value"], b["kc"], b["vc"], b["sm"],
+                                        w.k_scale, w.v_scale, stream=stream)
+            pa.pa_decode_fp8(b["out"], b["q"], b["kc"], b["vc"], b["bt"], b["cl"], w.scale,
+                             w.k_scale, w.v_scale, maxctx, ps, workspace=ws, stream=stream)
+        else:
+            pa.pa_reshape_and_cache(b["key"], b["value"], b["kc"], b["vc"], b["sm"],
+                                    stream=stream)
+            pa.pa_decode(b["out"], b["q"], b["kc"], b["vc"], b["bt"], b["cl"], w.scale, maxctx,
+                         ps, workspace=ws, stream=stream)
+
+    # eager reference results for both input sets
+    eager = {}
+    for name, w in (("base", base), ("other", other)):
+        b = buffers(w)
+        step(b, w)
+        torch.cuda.synchronize()
+        eager[name] = (b["out"].clone(), b["kc"].clone(), b["vc"].clone())
+
+    # capture with the base inputs in static buffers
+    static = buffers(base)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(static, base, stream=side)        # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    fresh = buffers(base)
+    for k in ("kc", "vc"):
+        static[k].copy_(fresh[k])
+    with torch.cuda.graph(g):
+        step(static, base, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    out, kc, vc = eager["base"]
+    assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16))
+    assert torch.equal(static["kc"], kc) and torch.equal(static["vc"], vc)
+
+    # new inputs in the same buffers, replay
+    nb = buffers(other)
+    for k in ("kc", "vc", "key", "value", "sm", "q", "bt", "cl"):
+        static[k].copy_(nb[k])
+    g.replay()
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() == 0
+    out, kc, vc = eager["other"]
+    assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16))
+    assert torch.equal(static["kc"], kc) and torch.equal(static["vc"], vc)

@@ -1,0 +1,90 @@
+"""GPU parity of chunked-prefill attention (pa_prefill) against the oracle:
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| per element, for every chunk row, after
+the chunk's K/V went into the pool through pa_reshape_and_cache."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+RTOL, ATOL = 1e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def pa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from pagedattention_kv_cache_attention_gb300 import build
+    build.build()
+    import pagedattention_kv_cache_attention_gb300 as pa
+    pa._load()
+    assert pa.pa_device_errors() == 0
+    return pa
+
+
+def run(pa, pw):
+    dev = torch.device("cuda")
+    kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
+    pa.pa_reshape_and_cache(pw.key.to(dev), pw.value.to(dev), kc, vc, pw.slot_mapping.to(dev))
+    q = pw.query.to(dev)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_prefill(out, q, pw.query_start.to(dev), kc, vc, pw.block_tables.to(dev),
+                  pw.context_lens.to(dev), pw.scale, pw.max_q_len)
+    torch.cuda.synchronize()
+    return kc, vc, out, pa.pa_device_errors()
+
+
+def check(pw, kc, vc, out, rows=None):
+    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
+    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.prefill(pw.query, pw.query_start, kh, vh, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype)
+    got = out.float().cpu().double().numpy()
+    if rows is not None:
+        ref, got = ref[rows], got[rows]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), f"{int(bad.sum())} elements outside tolerance, max err {err.max():.3g}"
+
+
+CASES = [
+    ("tiny_mha", dict(lens=[20, 37, 1, 64], chunk=9)),
+    ("tiny_mha", dict(lens=[30, 17], chunk=10**6)),                              # whole prompts
+    ("tiny_mha", dict(lens=[50, 3, 100], q_lens=[1, 1, 1])),                    # decode-like
+    ("tiny_mha", dict(lens=[70, 33], chunk=40, head_dim=128, dtype="bf16")),
+    ("llama3_8b_gqa", dict(lens=[600, 1500, 33], chunk=300)),                     # G = 4
+    ("llama3_8b_gqa", dict(lens=[200, 90], chunk=77, num_q_heads=24, num_kv_heads=8)),  # G = 3
+    ("llama3_70b_cb", dict(lens=[130, 1000, 31], chunk=65)),                      # G = 8, bs 32
+    ("llama3_70b_cb", dict(lens=[300, 64], chunk=10**6, head_dim=64, dtype="bf16")),
+    ("llama3_8b_gqa", dict(lens=[100, 40], chunk=10**6, num_q_heads=8, num_kv_heads=8)),  # G = 1
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(CASES)])
+def test_prefill_cases(pa, name, kw):
+    pw = W.make_prefill(name, 61, **kw)
+    kc, vc, out, err = run(pa, pw)
+    assert err == 0
+    check(pw, kc, vc, out)
+
+
+def test_prefill_llama3_8b_chunks_sampled(pa):
+    """Llama-3-8B shape: 16 sequences, 512-token chunks at the end of
+    contexts up to 4096; a seeded sample of rows is checked."""
+    pw = W.make_prefill("llama3_8b_gqa", 62, batch=16, chunk=512)
+    kc, vc, out, err = run(pa, pw)
+    assert err == 0
+    rows = np.random.default_rng(0).choice(pw.total_q, 400, replace=False)
+    check(pw, kc, vc, out, rows=np.sort(rows))
+
+
+def test_prefill_bad_length_flagged(pa):
+    pw = W.make_prefill("tiny_mha", 63, lens=[20, 30], chunk=10)
+    pw.context_lens[1] = 5          # shorter than its chunk
+    kc, vc, out, err = run(pa, pw)
+    assert err & pa.DEVERR_BAD_LEN
+    q0 = int(pw.query_start[0])
+    assert torch.isfinite(out[q0:q0 + 10].float()).all()

@@ -499,6 +499,86 @@ def pin_fp8_decode_equals_16bit_when_exact():
     assert np.allclose(a, 3.0 * b, rtol=1e-13, atol=1e-14)
 
 
+# ------------------------------------------------------- chunked prefill
+
+def _prefill_pool(pw):
+    kc = pw.k_cache.clone().view(torch.int16).numpy().view(np.uint16)
+    vc = pw.v_cache.clone().view(torch.int16).numpy().view(np.uint16)
+    oracle.reshape_and_cache(pw.key, pw.value, kc, vc, pw.slot_mapping)
+    return kc, vc
+
+
+def pin_prefill_single_token_is_decode():
+    """A chunk of one token is a decode step: bit-identical outputs."""
+    pw = W.make_prefill("llama3_8b_gqa", 20, lens=[5, 17, 40, 333], head_dim=64,
+                        num_q_heads=8, num_kv_heads=2, q_lens=[1, 1, 1, 1])
+    kc, vc = _prefill_pool(pw)
+    got = oracle.prefill(pw.query, pw.query_start, kc, vc, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype)
+    ref = oracle.decode(pw.query, kc, vc, pw.block_tables, pw.context_lens, pw.scale, pw.dtype)
+    assert np.array_equal(got, ref)
+
+
+def pin_prefill_rows_are_truncated_decodes():
+    """Row t of a chunk attends to exactly the tokens up to its position."""
+    pw = W.make_prefill("tiny_mha", 21, lens=[20, 37], chunk=9)
+    kc, vc = _prefill_pool(pw)
+    got = oracle.prefill(pw.query, pw.query_start, kc, vc, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype)
+    for i in range(pw.num_seqs):
+        ql = int(pw.q_lens[i])
+        for t in range(ql):
+            row = int(pw.query_start[i]) + t
+            pos = int(pw.context_lens[i]) - ql + t
+            ref = oracle.decode(pw.query[row:row + 1], kc, vc, pw.block_tables[i:i + 1],
+                                np.array([pos + 1], np.int32), pw.scale, pw.dtype)
+            assert np.array_equal(got[row], ref[0])
+
+
+def pin_prefill_vs_torch_causal_sdpa():
+    """Whole-prompt prefill (chunk = context) against torch's fp64
+    scaled_dot_product_attention with a causal mask on contiguous K/V."""
+    F = torch.nn.functional
+    pw = W.make_prefill("llama3_70b_cb", 22, lens=[50, 33], head_dim=64, num_q_heads=8,
+                        num_kv_heads=2, chunk=10**6)
+    kc, vc = _prefill_pool(pw)
+    got = oracle.prefill(pw.query, pw.query_start, kc, vc, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype)
+    G = 4
+    for i in range(pw.num_seqs):
+        c = int(pw.context_lens[i])
+        K = torch.from_numpy(np.stack([_contiguous_np(kc, pw.block_tables[i].numpy(), c, h, "fp16")
+                                       for h in range(2)])).repeat_interleave(G, 0)
+        V = torch.from_numpy(np.stack([_contiguous_np(vc, pw.block_tables[i].numpy(), c, h, "fp16")
+                                       for h in range(2)])).repeat_interleave(G, 0)
+        q0 = int(pw.query_start[i])
+        Q = pw.query[q0:q0 + c].double().permute(1, 0, 2)
+        ref = F.scaled_dot_product_attention(Q[None], K[None], V[None], is_causal=True,
+                                             scale=float(np.float32(pw.scale)))[0]
+        assert np.allclose(got[q0:q0 + c], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_prefill_chunks_compose():
+    """Prefilling a prompt in two chunks gives, row for row, the outputs of
+    prefilling it in one (bit-identical)."""
+    full = W.make_prefill("tiny_mha", 23, lens=[45, 30, 60, 17], chunk=10**6)
+    kc, vc = _prefill_pool(full)
+    one = oracle.prefill(full.query, full.query_start, kc, vc, full.block_tables,
+                         full.context_lens, full.scale, full.dtype)
+    ctx = full.context_lens.numpy()
+    cut = ctx // 2
+    for part in range(2):
+        lens = cut if part == 0 else ctx
+        ql = cut if part == 0 else ctx - cut
+        rows = np.concatenate([np.arange(int(full.query_start[i]) + (0 if part == 0 else cut[i]),
+                                         int(full.query_start[i]) + (cut[i] if part == 0 else ctx[i]))
+                               for i in range(full.num_seqs)])
+        qs = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        two = oracle.prefill(full.query[torch.from_numpy(rows)], qs, kc, vc, full.block_tables,
+                             lens.astype(np.int32), full.scale, full.dtype)
+        assert np.array_equal(two, one[rows])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

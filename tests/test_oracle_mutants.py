@@ -40,6 +40,9 @@ MUTANTS = [
     ("fp8_k_scale_dropped", "int rc = pa_oracle_gather(K, k_cache, kv_dtype, k_scale,",
      "int rc = pa_oracle_gather(K, k_cache, kv_dtype, 1.0,"),
     ("fp8_scatter_scale", "/ k_scale;", "* k_scale;"),
+    ("prefill_not_causal_inclusive", "int n = pos + 1;", "int n = pos;"),
+    ("prefill_position", "int pos = ctx - q_len + (row - query_start[i]);",
+     "int pos = ctx - q_len + (row - query_start[i]) / 2;"),
 ]
 
 RUNNER = r"""

@@ -307,3 +307,59 @@ def make(name: str, seed: int = 0, *, dtype: Optional[str] = None, batch: Option
                       partition_size if partition_size is not None else 1024, rng, gen,
                       table_len=max_len or 16384)
     raise KeyError(f"unknown workload {name!r}; known: {NAMES}")
+
+
+@dataclasses.dataclass
+class PrefillWorkload(Workload):
+    """A chunked-prefill batch: sequence i appends q_lens[i] new tokens, which
+    end its context (positions ctx_i - q_len_i .. ctx_i - 1).  query, key,
+    value are [total_q, heads, d] packed by sequence; query_start [B+1] gives
+    each sequence's first row; slot_mapping [total_q] each new token's slot.
+    Every chunk slot holds the poison value until the scatter writes it."""
+    query_start: torch.Tensor = None   # int32 [B + 1]
+    q_lens: torch.Tensor = None        # int32 [B]
+
+    @property
+    def total_q(self) -> int:
+        return int(self.query_start[-1].item())
+
+    @property
+    def max_q_len(self) -> int:
+        return int(self.q_lens.max().item()) if self.num_seqs else 0
+
+
+def make_prefill(name: str, seed: int = 0, *, chunk: int = 512,
+                 q_lens: Optional[Sequence[int]] = None, **kw) -> PrefillWorkload:
+    """A decode workload turned into a chunked-prefill batch: sequence i's
+    last min(chunk, ctx_i) tokens (or q_lens[i]) are the new chunk."""
+    w = make(name, seed, **kw)
+    ctx = w.context_lens.numpy().astype(np.int64)
+    ql = (np.minimum(ctx, chunk) if q_lens is None else np.asarray(q_lens, np.int64))
+    ql = np.minimum(ql, ctx)
+    qs = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    total = int(qs[-1])
+    bs = w.block_size
+    bt = w.block_tables.numpy()
+    slots = np.empty(total, np.int64)
+    for i in range(w.num_seqs):
+        for t in range(int(ql[i])):
+            pos = int(ctx[i] - ql[i] + t)
+            slots[qs[i] + t] = int(bt[i, pos // bs]) * bs + pos % bs
+    # the chunk's slots are poisoned until the scatter writes them
+    if total:
+        blk = torch.from_numpy(slots // bs)
+        off = torch.from_numpy(slots % bs)
+        for cache in (w.k_cache, w.v_cache):
+            v = cache[blk, :, off, :]
+            _poison(v, w.dtype)
+            cache[blk, :, off, :] = v
+    gen = torch.Generator().manual_seed(seed + 7919)
+    return PrefillWorkload(
+        **{f.name: getattr(w, f.name) for f in dataclasses.fields(Workload)
+           if f.name not in ("query", "key", "value", "slot_mapping")},
+        query=_randn((total, w.num_q_heads, w.head_dim), gen, w.dtype),
+        key=_randn((total, w.num_kv_heads, w.head_dim), gen, w.dtype),
+        value=_randn((total, w.num_kv_heads, w.head_dim), gen, w.dtype),
+        slot_mapping=torch.from_numpy(slots),
+        query_start=torch.from_numpy(qs), q_lens=torch.from_numpy(ql.astype(np.int32)))
+
