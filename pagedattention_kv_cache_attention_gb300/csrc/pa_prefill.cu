@@ -372,6 +372,9 @@ cudaError_t launch_prefill_t(const PrefillArgs &a, const CUtensorMap &km, const 
 
 bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
                      bool fp8);
+bool prefill_tc_supported(int head_dim, int group);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+                              int dtype, cudaStream_t stream);
 
 constexpr int kPrefillWarps = 4;
 constexpr int kPrefillStages = 4;
@@ -387,6 +390,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void
     return cudaErrorInvalidValue;
   }
   if (a.max_q_len == 0) return cudaSuccess;
+  // head_dim 128 with a power-of-two group runs on the tcgen05 kernel
+  if (a.use_tc && prefill_tc_supported(head_dim, a.group))
+    return launch_prefill_tc(a, km, vm, dtype, stream);
   if (dtype == 0)
     return head_dim == 128
                ? launch_prefill_t<__half, 128, kPrefillWarps, kPrefillStages>(a, km, vm, stream)

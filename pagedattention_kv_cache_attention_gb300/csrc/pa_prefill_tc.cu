@@ -1,0 +1,433 @@
+// pa_prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
+// core (tcgen05: operands in shared memory, accumulators in tensor memory).
+//
+// Same computation as pa_prefill.cu ("Serving engines", How vLLM works:
+// chunked prefill; chunk row t at position ctx - q_len + t attends causally to
+// tokens 0..t's position through the block table), for head_dim 128 and query
+// groups G in {1, 2, 4, 8}.
+//
+// One CTA per (128 query rows, KV head, sequence); the rows are 128/G tokens x
+// G heads of one KV group.  Warp roles:
+//  * warps 0-3 (128 threads): thread r owns query row r and TMEM lane r.  They
+//    stage Q (128-byte-swizzled, K-major) once, then per 64-key step read the
+//    scores row from TMEM, apply the causal mask, run the online softmax and
+//    write P (fp16/bf16, swizzled K-major) to shared memory.  The running max
+//    is only moved -- and O in TMEM rescaled -- when a row's max grows by more
+//    than 2^8; between moves P may exceed 1 (at most 256), which fp16/bf16
+//    carry exactly as far as their precision goes, and numerator and
+//    denominator share the same reference.  In the last step they zero V rows
+//    past the keys in use, so tail slots (whatever they hold) cannot reach O.
+//  * warp 4, one thread: issues S = Q K^T (M 128, N 64, K 128: 8 MMAs) into
+//    one of two TMEM score buffers and O += P V (M 128, N 128, K 64: 4 MMAs,
+//    V as an MN-major operand) into the TMEM output, committing each to an
+//    mbarrier.  S for step j+1 is issued before P V of step j, so the tensor
+//    core works while the softmax warps do.
+//  * warp 5, one thread: stages 64-key K/V steps (4 sub-tiles of 16 rows, two
+//    128-byte boxes each for K and V) through the block table with 2-D TMA into
+//    a ring of S stages, refilling a stage once the P V product that read it
+//    has completed.
+// TMEM: scores in columns 0-127 (two buffers of 64), O in columns 128-255.
+// bf16 carries P as hi + lo parts (two P V MMAs), so P keeps ~16 bits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kTcRows = 128;     // query rows per CTA = TMEM lanes
+constexpr int kTcKeys = 64;      // keys per step
+constexpr int kTcDim = 128;      // head_dim
+constexpr int kAtomRows128 = kTcRows * 128;  // one 64-dim atom of 128 rows (bytes)
+constexpr int kAtomRows64 = kTcKeys * 128;   // one 64-dim atom of 64 key rows (bytes)
+constexpr float kRescaleLog2 = 8.f;         // move the running max only past this growth
+constexpr unsigned kFullMask = 0xffffffffu;
+
+template <typename T, int S, bool SPLIT>
+__global__ void __launch_bounds__(192, 1)
+    pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  constexpr int kQOff = 0;                                   // 2 atoms x 128 rows
+  constexpr int kPOff = 2 * kAtomRows128;                    // P hi: 128 rows x 64 keys
+  constexpr int kPLoOff = kPOff + kAtomRows128;              // P lo (SPLIT)
+  constexpr int kStageOff = kPOff + (SPLIT ? 2 : 1) * kAtomRows128;
+  constexpr int kStageBytes = 4 * kAtomRows64;               // K: 2 atoms, V: 2 atoms
+  constexpr int kBarOff = kStageOff + S * kStageBytes;
+  constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
+  uint64_t *kv_empty = kv_full + S;
+  uint64_t *s_full = kv_empty + S;  // [2]
+  uint64_t *p_full = s_full + 2;
+  uint64_t *pv_done = p_full + 1;
+  uint64_t *q_ready = pv_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
+  uint32_t *step_valid = tmem_slot + 1;  // [S]: bit h = sub-tile h of the step was loaded
+
+  const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.group;
+  const int tpc = kTcRows / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, kTcRows);
+    mbar_init(pv_done, 1);
+    mbar_init(q_ready, kTcRows);
+    fence_barrier_init();
+  }
+  if (warp == 4) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();  // the chunk's K/V may come from the kernel before
+
+  const int q0 = a.query_start[seq];
+  const int q_len = a.query_start[seq + 1] - q0;
+  const int ctx = a.context_lens[seq];
+  bool active = true;
+  if (q_len < 0 || ctx < q_len || ctx > (a.max_blocks_per_seq << a.bs_log2) ||
+      q_len > a.max_q_len) {
+    if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
+    active = false;
+  }
+  const int t_first = tile * tpc;
+  if (t_first >= q_len) active = false;
+  const int t_last = min(q_len, t_first + tpc) - 1;
+  const int base_pos = ctx - q_len;
+  const int n_keys = base_pos + t_last + 1;
+  const int n_steps = active ? (n_keys + kTcKeys - 1) / kTcKeys : 0;
+
+  if (active && warp < 4) {
+    // ------------------------------------------------------------ softmax warps
+    const int r = tid;
+    const int tok = t_first + r / G;
+    const bool row_ok = r < tpc * G && tok <= t_last;
+    const int pos = base_pos + tok;
+    {
+      const T *qrow = static_cast<const T *>(a.query) +
+                      (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
+                       r % G) * kTcDim;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
+                               : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + kQOff + (ch >> 3) * kAtomRows128 + r * 128 +
+                                   (((ch & 7) ^ (r & 7)) << 4)) = v;
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(q_ready);
+
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok_run = true;
+    for (int j = 0; j < n_steps && ok_run; ++j) {
+      const int s = j % S;
+      // warp-uniform decisions: the TMEM loads and stores below are warp-collective
+      const bool got = mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1) &&
+                       mbar_wait_bounded(&kv_full[s], (j / S) & 1);
+      if (!__all_sync(kFullMask, got)) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        ok_run = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64];
+      {
+        float t0[32], t1[32];
+        tmem_ld32(lane_addr + (j & 1) * kTcKeys, t0);
+        tmem_ld32(lane_addr + (j & 1) * kTcKeys + 32, t1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = t0[i];
+          sv[32 + i] = t1[i];
+        }
+      }
+      const int key0 = j * kTcKeys;
+      const uint32_t vmask = step_valid[s];
+      // zero V rows this step must not use: past the keys in use, or never loaded
+      if (key0 + kTcKeys > n_keys || vmask != 0xFu) {
+        const int kr = r >> 1, atom = r & 1;
+        if (key0 + kr >= n_keys || !((vmask >> (kr >> 4)) & 1u)) {
+          uint4 *row = reinterpret_cast<uint4 *>(smem + kStageOff + s * kStageBytes +
+                                                 (2 + atom) * kAtomRows64 + kr * 128);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int key = key0 + c;
+        const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
+        sv[c] = ok ? sv[c] * a.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, sv[c]);
+      }
+      // P V of the previous step read P and wrote O: wait for it before touching either
+      if (j > 0 && !__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        ok_run = false;
+        break;
+      }
+      tc_fence_after();
+      const float m_new = fmaxf(m_ref, tmax);
+      const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
+      const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new));
+      if (move) {
+        l *= alpha;
+        m_ref = m_new;
+      }
+      if (j > 0 && __any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float o[32];
+          tmem_ld32(lane_addr + 128 + cb * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_addr + 128 + cb * 32, o);
+        }
+        tmem_wait_st();
+      }
+      // P row: 64 keys, eight 16-byte chunks (swizzled); bf16 also writes the remainders
+      const bool live = m_ref != -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = live ? exp2f(sv[ch * 8 + 2 * e] - m_ref) : 0.f;
+          const float p1 = live ? exp2f(sv[ch * 8 + 2 * e + 1] - m_ref) : 0.f;
+          l += p0 + p1;
+          hi[e] = Elem<T>::pack(p0, p1);
+          if constexpr (SPLIT) {
+            const float2 f = Elem<T>::unpack(hi[e]);
+            lo[e] = Elem<T>::pack(p0 - f.x, p1 - f.y);
+          }
+        }
+        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4 *>(smem + kPOff + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        if constexpr (SPLIT)
+          *reinterpret_cast<uint4 *>(smem + kPLoOff + off) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // ---- epilogue: O / l for this row
+    if (ok_run && n_steps > 0) {
+      if (__all_sync(kFullMask, mbar_wait_bounded(pv_done, (n_steps - 1) & 1))) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T *orow = static_cast<T *>(a.out) +
+                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + r % G) * kTcDim;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float o[32];
+          tmem_ld32(lane_addr + 128 + cb * 32, o);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 pk;
+              pk.x = Elem<T>::pack(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              pk.y = Elem<T>::pack(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              pk.z = Elem<T>::pack(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              pk.w = Elem<T>::pack(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              *reinterpret_cast<uint4 *>(orow + cb * 32 + q * 8) = pk;
+            }
+          }
+        }
+      } else if (lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
+  } else if (active && warp == 4) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kTcKeys);
+      const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
+      const uint32_t sq = smem_addr(smem + kQOff), sp = smem_addr(smem + kPOff);
+      const uint32_t splo = smem_addr(smem + kPLoOff);
+      const uint32_t sst = smem_addr(smem + kStageOff);
+      bool ok_run = mbar_wait_bounded(q_ready, 0);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % S;
+        if (!mbar_wait_bounded(&kv_full[s], (j / S) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = sst + s * kStageBytes;
+#pragma unroll
+        for (int k = 0; k < kTcDim / 16; ++k) {
+          const uint64_t da = umma_desc_sw128(sq + (k >> 2) * kAtomRows128 + (k & 3) * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kAtomRows64 + (k & 3) * 32, 16, 1024);
+          umma_f16(tmem + (j & 1) * kTcKeys, da, db, id_qk, k > 0);
+        }
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok_run) ok_run = issue_qk(0);
+      for (int j = 0; j < n_steps && ok_run; ++j) {
+        if (j + 1 < n_steps && !issue_qk(j + 1)) {
+          ok_run = false;
+          break;
+        }
+        if (!mbar_wait_bounded(p_full, j & 1)) {
+          ok_run = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = sst + (j % S) * kStageBytes + 2 * kAtomRows64;
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          const uint64_t da = umma_desc_sw128(sp + kk * 32, 16, 1024);
+          const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
+          umma_f16(tmem + 128, da, dv, id_pv, j > 0 || kk > 0);
+        }
+        if constexpr (SPLIT) {
+#pragma unroll
+          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+            const uint64_t da = umma_desc_sw128(splo + kk * 32, 16, 1024);
+            const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
+            umma_f16(tmem + 128, da, dv, id_pv, true);
+          }
+        }
+        umma_commit(pv_done);
+        umma_commit(&kv_empty[j % S]);
+      }
+      if (!ok_run) atomicOr(a.err, kErrTimeout);
+    }
+  } else if (active && warp == 5) {
+    // ---------------------------------------------------------- TMA producer
+    const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
+    const int n_sub = (n_keys + 15) / 16;
+    const int bs_mask = (1 << a.bs_log2) - 1;
+    auto block_of = [&](int u) -> int {
+      if (u >= n_sub) return -1;
+      const int phys = bt_row[(u * 16) >> a.bs_log2];
+      if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
+        atomicOr(a.err, kErrBadBlock);
+        return -1;
+      }
+      return phys;
+    };
+    const uint64_t policy = l2_policy_evict_first();
+    int win_base = 0;
+    int win = block_of(lane);
+    bool ok_run = true;
+    for (int j = 0; j < n_steps && ok_run; ++j) {
+      const int s = j % S;
+      if (j * 4 >= win_base + 32) {
+        win_base += 32;
+        win = block_of(win_base + lane);
+      }
+      int phys[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) phys[h] = __shfl_sync(kFullMask, win, j * 4 + h - win_base);
+      if (lane == 0) {
+        if (j >= S && !mbar_wait_bounded(&kv_empty[s], ((j / S) - 1) & 1)) {
+          atomicOr(a.err, kErrTimeout);
+          ok_run = false;
+        } else {
+          uint32_t mask = 0, bytes = 0;
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            if (phys[h] >= 0) {
+              mask |= 1u << h;
+              bytes += 4 * 2048;
+            }
+          step_valid[s] = mask;
+          if (bytes == 0) {
+            mbar_arrive(&kv_full[s]);
+          } else {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&kv_full[s], bytes);
+            uint8_t *st = smem + kStageOff + s * kStageBytes;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (phys[h] < 0) continue;
+              const int u = j * 4 + h;
+              const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                tma_load_2d(st + b * kAtomRows64 + h * 2048, &kmap, b * 64, y, &kv_full[s], policy);
+                tma_load_2d(st + (2 + b) * kAtomRows64 + h * 2048, &vmap, b * 64, y, &kv_full[s],
+                            policy);
+              }
+            }
+          }
+        }
+      }
+      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+    }
+  }
+
+  // ---- teardown: every tcgen05 operation is complete once pv_done's last
+  // phase has been observed by the softmax warps (or the CTA had no work)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+  grid_launch_dependents();
+}
+
+template <typename T, int S, bool SPLIT>
+cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+                                cudaStream_t stream) {
+  constexpr size_t smem = 1024 + 2 * kAtomRows128 + (SPLIT ? 2 : 1) * kAtomRows128 +
+                          static_cast<size_t>(S) * 4 * kAtomRows64 + (2 * S + 5) * 8 + 8 + S * 4;
+  auto kern = pa_prefill_tc_kernel<T, S, SPLIT>;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int tpc = kTcRows / a.group;
+  const int tiles = (a.max_q_len + tpc - 1) / tpc;
+  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(192), smem, stream,
+                          km, vm, a);
+}
+
+}  // namespace
+
+#ifndef PA_PREFILL_TC_STAGES
+#define PA_PREFILL_TC_STAGES 3
+#endif
+
+bool prefill_tc_supported(int head_dim, int group) {
+  return head_dim == kTcDim && (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+                              int dtype, cudaStream_t stream) {
+  if (dtype == 0) return launch_prefill_tc_t<__half, PA_PREFILL_TC_STAGES, false>(a, km, vm, stream);
+  return launch_prefill_tc_t<__nv_bfloat16, PA_PREFILL_TC_STAGES, true>(a, km, vm, stream);
+}
+
+}  // namespace pa
