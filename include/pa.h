@@ -184,8 +184,9 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
  * query, out     device, [total_q, num_q_heads, head_dim], dtype; 16-byte aligned
  * query_start    device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
  * max_q_len      >= every q_len_i (sizes the launch)
- * Softmax and accumulation fp32; out rounded to dtype.  head_dim in {64, 128},
- * block_size in {16, 32}, num_q_heads / num_kv_heads in 1..8.  A q_len_i
+ * Softmax and accumulation fp32; out rounded to dtype.  scale > 0.  head_dim
+ * in {64, 128}, block_size in {16, 32}, num_q_heads / num_kv_heads in 1..8
+ * (head_dim 128 with a group of 1, 2, 4 or 8 runs on the tcgen05 kernel).  A q_len_i
  * larger than context_lens[i] or than max_q_len, or a context longer than the
  * table, skips that sequence and sets PA_DEVERR_BAD_LEN.
  */

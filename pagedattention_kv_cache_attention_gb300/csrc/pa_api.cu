@@ -322,7 +322,8 @@ pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
                      int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
                      int32_t dtype, void *stream) {
   if (num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-      num_blocks <= 0 || max_blocks_per_seq <= 0 || !dtype_ok(dtype) || !std::isfinite(scale))
+      num_blocks <= 0 || max_blocks_per_seq <= 0 || !dtype_ok(dtype) || !std::isfinite(scale) ||
+      !(scale > 0.f))
     return PA_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
   const int32_t group = num_q_heads / num_kv_heads;

@@ -204,6 +204,14 @@ __device__ __forceinline__ uint32_t interleave_bytes(const uint4 &x, const uint4
                      b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12));
 }
 
+// 2^x by the PTX approximate base-2 exponential (flushes subnormal results
+// to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Fifth-generation tensor core: MMA operands in shared memory (described by
 // 64-bit matrix descriptors), accumulators in tensor memory (TMEM).

@@ -11,7 +11,9 @@
 //  * warps 0-3 (128 threads): thread r owns query row r and TMEM lane r.  They
 //    stage Q (128-byte-swizzled, K-major) once, then per 64-key step read the
 //    scores row from TMEM, apply the causal mask, run the online softmax and
-//    write P (fp16/bf16, swizzled K-major) to shared memory.  The running max
+//    write P (fp16/bf16, swizzled K-major) to shared memory: one FFMA and one
+//    ex2.approx per score, masks only on steps that cross a row's position,
+//    tree reductions for the row max and sum.  The running max
 //    is only moved -- and O in TMEM rescaled -- when a row's max grows by more
 //    than 2^8; between moves P may exceed 1 (at most 256), which fp16/bf16
 //    carry exactly as far as their precision goes, and numerator and
@@ -173,14 +175,26 @@ __global__ void __launch_bounds__(192, 1)
           for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
         }
       }
-      float tmax = -INFINITY;
+      // mask (only steps that reach past the row's position or hold an
+      // unloaded sub-tile need it) and the row max of the raw scores
+      const bool full_step = row_ok && key0 + kTcKeys - 1 <= pos && vmask == 0xFu;
+      if (!full_step) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int key = key0 + c;
-        const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
-        sv[c] = ok ? sv[c] * a.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, sv[c]);
+        for (int c = 0; c < 64; ++c) {
+          const int key = key0 + c;
+          const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
+          sv[c] = ok ? sv[c] : -INFINITY;
+        }
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx[i] = fmaxf(fmaxf(fmaxf(sv[8 * i], sv[8 * i + 1]), fmaxf(sv[8 * i + 2], sv[8 * i + 3])),
+                      fmaxf(fmaxf(sv[8 * i + 4], sv[8 * i + 5]), fmaxf(sv[8 * i + 6], sv[8 * i + 7])));
+      }
+      const float tmax_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float tmax = tmax_raw * a.scale_log2;  // the scale is positive: same order
       // P V of the previous step read P and wrote O: wait for it before touching either
       if (j > 0 && !__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
         if (lane == 0) atomicOr(a.err, kErrTimeout);
@@ -190,7 +204,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const float m_new = fmaxf(m_ref, tmax);
       const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
-      const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new));
+      const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - m_new));
       if (move) {
         l *= alpha;
         m_ref = m_new;
@@ -207,20 +221,23 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_wait_st();
       }
-      // P row: 64 keys, eight 16-byte chunks (swizzled); bf16 also writes the remainders
-      const bool live = m_ref != -INFINITY;
+      // P = 2^(s scale - m): one FFMA and one ex2 per score; a row with no key
+      // yet (m = -inf) gets 2^-inf = 0 everywhere
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      float ls[8];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(fmaf(sv[ch * 8 + e], a.scale_log2, neg_m));
+        ls[ch] = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = live ? exp2f(sv[ch * 8 + 2 * e] - m_ref) : 0.f;
-          const float p1 = live ? exp2f(sv[ch * 8 + 2 * e + 1] - m_ref) : 0.f;
-          l += p0 + p1;
-          hi[e] = Elem<T>::pack(p0, p1);
+          hi[e] = Elem<T>::pack(pv[2 * e], pv[2 * e + 1]);
           if constexpr (SPLIT) {
             const float2 f = Elem<T>::unpack(hi[e]);
-            lo[e] = Elem<T>::pack(p0 - f.x, p1 - f.y);
+            lo[e] = Elem<T>::pack(pv[2 * e] - f.x, pv[2 * e + 1] - f.y);
           }
         }
         const int off = r * 128 + ((ch ^ (r & 7)) << 4);
@@ -229,6 +246,7 @@ __global__ void __launch_bounds__(192, 1)
           *reinterpret_cast<uint4 *>(smem + kPLoOff + off) =
               make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
