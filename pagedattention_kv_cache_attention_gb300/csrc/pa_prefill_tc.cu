@@ -19,16 +19,18 @@
 //    carry exactly as far as their precision goes, and numerator and
 //    denominator share the same reference.  In the last step they zero V rows
 //    past the keys in use, so tail slots (whatever they hold) cannot reach O.
-//  * warp 4, one thread: issues S = Q K^T (M 128, N 64, K 128: 8 MMAs) into
-//    one of two TMEM score buffers and O += P V (M 128, N 128, K 64: 4 MMAs,
+//  * warp 4, one thread: issues S = Q K^T (M 128, N = KEYS, K 128: 8 MMAs)
+//    into one of two TMEM score buffers and O += P V (M 128, N 128, K = KEYS,
 //    V as an MN-major operand) into the TMEM output, committing each to an
 //    mbarrier.  S for step j+1 is issued before P V of step j, so the tensor
 //    core works while the softmax warps do.
-//  * warp 5, one thread: stages 64-key K/V steps (4 sub-tiles of 16 rows, two
+//  * warp 5, one thread: stages KEYS-key K/V steps (16-row sub-tiles, two
 //    128-byte boxes each for K and V) through the block table with 2-D TMA into
 //    a ring of S stages, refilling a stage once the P V product that read it
 //    has completed.
-// TMEM: scores in columns 0-127 (two buffers of 64), O in columns 128-255.
+// KEYS = 32 and S = 3 keep a CTA under half of the SM's shared memory, so two
+// CTAs run per SM (measured 694 vs 526 TFLOP/s for one CTA with 64-key steps).
+// TMEM: scores in columns 0..2 KEYS (two buffers), O in columns 128-255.
 // bf16 carries P as hi + lo parts (two P V MMAs), so P keeps ~16 bits.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -45,21 +47,26 @@ namespace pa {
 namespace {
 
 constexpr int kTcRows = 128;     // query rows per CTA = TMEM lanes
-constexpr int kTcKeys = 64;      // keys per step
 constexpr int kTcDim = 128;      // head_dim
 constexpr int kAtomRows128 = kTcRows * 128;  // one 64-dim atom of 128 rows (bytes)
-constexpr int kAtomRows64 = kTcKeys * 128;   // one 64-dim atom of 64 key rows (bytes)
 constexpr float kRescaleLog2 = 8.f;         // move the running max only past this growth
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <typename T, int S, bool SPLIT>
-__global__ void __launch_bounds__(192, 1)
+template <typename T, int S, bool SPLIT, int KEYS>
+__global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
     pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  constexpr int kTcKeys = KEYS;                 // keys per step
+  constexpr int kAtomRows64 = kTcKeys * 128;    // one 64-dim atom of the step's key rows (bytes)
+  constexpr int kSub = kTcKeys / 16;            // 16-row sub-tiles per step
+  constexpr uint32_t kAllSub = (1u << kSub) - 1;
+  // P rows have a 128-byte pitch; with 32-key steps the lo parts use the second
+  // half of each row (byte offset 64), otherwise a second tile
+  constexpr bool kLoInline = SPLIT && KEYS == 32;
   constexpr int kQOff = 0;                                   // 2 atoms x 128 rows
-  constexpr int kPOff = 2 * kAtomRows128;                    // P hi: 128 rows x 64 keys
-  constexpr int kPLoOff = kPOff + kAtomRows128;              // P lo (SPLIT)
-  constexpr int kStageOff = kPOff + (SPLIT ? 2 : 1) * kAtomRows128;
+  constexpr int kPOff = 2 * kAtomRows128;                    // P hi: 128 rows x KEYS keys
+  constexpr int kPLoOff = kPOff + kAtomRows128;              // P lo, own tile (KEYS == 64)
+  constexpr int kStageOff = kPOff + (SPLIT && !kLoInline ? 2 : 1) * kAtomRows128;
   constexpr int kStageBytes = 4 * kAtomRows64;               // K: 2 atoms, V: 2 atoms
   constexpr int kBarOff = kStageOff + S * kStageBytes;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
@@ -151,24 +158,21 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      float sv[64];
-      {
-        float t0[32], t1[32];
-        tmem_ld32(lane_addr + (j & 1) * kTcKeys, t0);
-        tmem_ld32(lane_addr + (j & 1) * kTcKeys + 32, t1);
+      float sv[kTcKeys];
+#pragma unroll
+      for (int q = 0; q < kTcKeys / 32; ++q) {
+        float t0[32];
+        tmem_ld32(lane_addr + (j & 1) * kTcKeys + 32 * q, t0);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = t0[i];
-          sv[32 + i] = t1[i];
-        }
+        for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
       }
       const int key0 = j * kTcKeys;
       const uint32_t vmask = step_valid[s];
       // zero V rows this step must not use: past the keys in use, or never loaded
-      if (key0 + kTcKeys > n_keys || vmask != 0xFu) {
+      if (key0 + kTcKeys > n_keys || vmask != kAllSub) {
         const int kr = r >> 1, atom = r & 1;
-        if (key0 + kr >= n_keys || !((vmask >> (kr >> 4)) & 1u)) {
+        if (kr < kTcKeys && (key0 + kr >= n_keys || !((vmask >> (kr >> 4)) & 1u))) {
           uint4 *row = reinterpret_cast<uint4 *>(smem + kStageOff + s * kStageBytes +
                                                  (2 + atom) * kAtomRows64 + kr * 128);
 #pragma unroll
@@ -177,31 +181,28 @@ __global__ void __launch_bounds__(192, 1)
       }
       // mask (only steps that reach past the row's position or hold an
       // unloaded sub-tile need it) and the row max of the raw scores
-      const bool full_step = row_ok && key0 + kTcKeys - 1 <= pos && vmask == 0xFu;
+      const bool full_step = row_ok && key0 + kTcKeys - 1 <= pos && vmask == kAllSub;
       if (!full_step) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < kTcKeys; ++c) {
           const int key = key0 + c;
           const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
           sv[c] = ok ? sv[c] : -INFINITY;
         }
       }
+      constexpr int kCh = kTcKeys / 8;  // 8-score chunks (16 bytes of P each)
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mx[i] = fmaxf(fmaxf(fmaxf(sv[8 * i], sv[8 * i + 1]), fmaxf(sv[8 * i + 2], sv[8 * i + 3])),
-                      fmaxf(fmaxf(sv[8 * i + 4], sv[8 * i + 5]), fmaxf(sv[8 * i + 6], sv[8 * i + 7])));
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kCh; ++i) {
+        mx[i & 7] = fmaxf(mx[i & 7],
+                          fmaxf(fmaxf(fmaxf(sv[8 * i], sv[8 * i + 1]), fmaxf(sv[8 * i + 2], sv[8 * i + 3])),
+                                fmaxf(fmaxf(sv[8 * i + 4], sv[8 * i + 5]), fmaxf(sv[8 * i + 6], sv[8 * i + 7]))));
       }
       const float tmax_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float tmax = tmax_raw * a.scale_log2;  // the scale is positive: same order
-      // P V of the previous step read P and wrote O: wait for it before touching either
-      if (j > 0 && !__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
-        if (lane == 0) atomicOr(a.err, kErrTimeout);
-        ok_run = false;
-        break;
-      }
-      tc_fence_after();
       const float m_new = fmaxf(m_ref, tmax);
       const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
       const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - m_new));
@@ -209,6 +210,37 @@ __global__ void __launch_bounds__(192, 1)
         l *= alpha;
         m_ref = m_new;
       }
+      // P = 2^(s scale - m): one FFMA and one ex2 per score; a row with no key
+      // yet (m = -inf) gets 2^-inf = 0 everywhere.  Packed in registers first,
+      // so the previous P V product has time to finish.
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      uint32_t ph[kCh * 4], pl[SPLIT ? kCh * 4 : 1];
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kCh; ++ch) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(fmaf(sv[ch * 8 + e], a.scale_log2, neg_m));
+        ls[ch & 7] += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ph[ch * 4 + e] = Elem<T>::pack(pv[2 * e], pv[2 * e + 1]);
+          if constexpr (SPLIT) {
+            const float2 f = Elem<T>::unpack(ph[ch * 4 + e]);
+            pl[ch * 4 + e] = Elem<T>::pack(pv[2 * e] - f.x, pv[2 * e + 1] - f.y);
+          }
+        }
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // P V of the previous step read P and wrote O: wait for it before touching either
+      if (j > 0 && !__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        ok_run = false;
+        break;
+      }
+      tc_fence_after();
       if (j > 0 && __any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
@@ -221,32 +253,18 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s scale - m): one FFMA and one ex2 per score; a row with no key
-      // yet (m = -inf) gets 2^-inf = 0 everywhere
-      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ls[8];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(fmaf(sv[ch * 8 + e], a.scale_log2, neg_m));
-        ls[ch] = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hi[e] = Elem<T>::pack(pv[2 * e], pv[2 * e + 1]);
-          if constexpr (SPLIT) {
-            const float2 f = Elem<T>::unpack(hi[e]);
-            lo[e] = Elem<T>::pack(pv[2 * e] - f.x, pv[2 * e + 1] - f.y);
-          }
-        }
+      for (int ch = 0; ch < kCh; ++ch) {
         const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4 *>(smem + kPOff + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if constexpr (SPLIT)
-          *reinterpret_cast<uint4 *>(smem + kPLoOff + off) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4 *>(smem + kPOff + off) =
+            make_uint4(ph[ch * 4], ph[ch * 4 + 1], ph[ch * 4 + 2], ph[ch * 4 + 3]);
+        if constexpr (SPLIT) {
+          const int lo_off = kLoInline ? kPOff + r * 128 + (((ch + 4) ^ (r & 7)) << 4)
+                                       : kPLoOff + off;
+          *reinterpret_cast<uint4 *>(smem + lo_off) =
+              make_uint4(pl[ch * 4], pl[ch * 4 + 1], pl[ch * 4 + 2], pl[ch * 4 + 3]);
+        }
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -323,7 +341,7 @@ __global__ void __launch_bounds__(192, 1)
         if constexpr (SPLIT) {
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint64_t da = umma_desc_sw128(splo + kk * 32, 16, 1024);
+            const uint64_t da = umma_desc_sw128((kLoInline ? sp + 64 : splo) + kk * 32, 16, 1024);
             const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
             umma_f16(tmem + 128, da, dv, id_pv, true);
           }
@@ -353,13 +371,13 @@ __global__ void __launch_bounds__(192, 1)
     bool ok_run = true;
     for (int j = 0; j < n_steps && ok_run; ++j) {
       const int s = j % S;
-      if (j * 4 >= win_base + 32) {
+      if (j * kSub >= win_base + 32) {
         win_base += 32;
         win = block_of(win_base + lane);
       }
-      int phys[4];
+      int phys[kSub];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) phys[h] = __shfl_sync(kFullMask, win, j * 4 + h - win_base);
+      for (int h = 0; h < kSub; ++h) phys[h] = __shfl_sync(kFullMask, win, j * kSub + h - win_base);
       if (lane == 0) {
         if (j >= S && !mbar_wait_bounded(&kv_empty[s], ((j / S) - 1) & 1)) {
           atomicOr(a.err, kErrTimeout);
@@ -367,7 +385,7 @@ __global__ void __launch_bounds__(192, 1)
         } else {
           uint32_t mask = 0, bytes = 0;
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
+          for (int h = 0; h < kSub; ++h)
             if (phys[h] >= 0) {
               mask |= 1u << h;
               bytes += 4 * 2048;
@@ -380,9 +398,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive_expect_tx(&kv_full[s], bytes);
             uint8_t *st = smem + kStageOff + s * kStageBytes;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < kSub; ++h) {
               if (phys[h] < 0) continue;
-              const int u = j * 4 + h;
+              const int u = j * kSub + h;
               const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
 #pragma unroll
               for (int b = 0; b < 2; ++b) {
@@ -409,12 +427,13 @@ __global__ void __launch_bounds__(192, 1)
   grid_launch_dependents();
 }
 
-template <typename T, int S, bool SPLIT>
+template <typename T, int S, bool SPLIT, int KEYS>
 cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                                 cudaStream_t stream) {
-  constexpr size_t smem = 1024 + 2 * kAtomRows128 + (SPLIT ? 2 : 1) * kAtomRows128 +
-                          static_cast<size_t>(S) * 4 * kAtomRows64 + (2 * S + 5) * 8 + 8 + S * 4;
-  auto kern = pa_prefill_tc_kernel<T, S, SPLIT>;
+  constexpr size_t smem = 1024 + 2 * kAtomRows128 +
+                          (SPLIT && KEYS != 32 ? 2 : 1) * kAtomRows128 +
+                          static_cast<size_t>(S) * 4 * KEYS * 128 + (2 * S + 5) * 8 + 8 + S * 4;
+  auto kern = pa_prefill_tc_kernel<T, S, SPLIT, KEYS>;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -434,8 +453,13 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 
 }  // namespace
 
+// 32-key steps x 3 stages keep a CTA under half the shared memory, so two
+// CTAs (two softmax warps per scheduler, two MMA streams) share an SM.
 #ifndef PA_PREFILL_TC_STAGES
 #define PA_PREFILL_TC_STAGES 3
+#endif
+#ifndef PA_PREFILL_TC_KEYS
+#define PA_PREFILL_TC_KEYS 32
 #endif
 
 bool prefill_tc_supported(int head_dim, int group) {
@@ -444,8 +468,11 @@ bool prefill_tc_supported(int head_dim, int group) {
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                               int dtype, cudaStream_t stream) {
-  if (dtype == 0) return launch_prefill_tc_t<__half, PA_PREFILL_TC_STAGES, false>(a, km, vm, stream);
-  return launch_prefill_tc_t<__nv_bfloat16, PA_PREFILL_TC_STAGES, true>(a, km, vm, stream);
+  if (dtype == 0)
+    return launch_prefill_tc_t<__half, PA_PREFILL_TC_STAGES, false, PA_PREFILL_TC_KEYS>(a, km, vm,
+                                                                                      stream);
+  return launch_prefill_tc_t<__nv_bfloat16, PA_PREFILL_TC_STAGES, true, PA_PREFILL_TC_KEYS>(a, km, vm,
+                                                                                           stream);
 }
 
 }  // namespace pa
