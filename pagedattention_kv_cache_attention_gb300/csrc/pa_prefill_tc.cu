@@ -1,5 +1,5 @@
 // pa_prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
-// core (tcgen05: operands in shared memory, accumulators in tensor memory).
+// core (tcgen05: accumulators and two of the operands in tensor memory).
 //
 // Same computation as pa_prefill.cu ("Serving engines", How vLLM works:
 // chunked prefill; chunk row t at position ctx - q_len + t attends causally to
@@ -7,31 +7,36 @@
 // groups G in {1, 2, 4, 8}.
 //
 // One CTA per (128 query rows, KV head, sequence); the rows are 128/G tokens x
-// G heads of one KV group.  Warp roles:
+// G heads of one KV group.  Q and P are the A operands of the two products and
+// live in tensor memory next to the accumulators, so shared memory only holds
+// the K/V ring and the tensor core reads just K and V from it (a 32-key step
+// reads 16 KB of shared memory instead of 56 KB with Q and P there).
+// Warp roles:
 //  * warps 0-3 (128 threads): thread r owns query row r and TMEM lane r.  They
-//    stage Q (128-byte-swizzled, K-major) once, then per 64-key step read the
-//    scores row from TMEM, apply the causal mask, run the online softmax and
-//    write P (fp16/bf16, swizzled K-major) to shared memory: one FFMA and one
+//    write Q into tensor memory once, then per KEYS-key step read the scores
+//    row, apply the causal mask, run the online softmax and write P
+//    (fp16/bf16 pairs) over the scores it came from: one FFMA and one
 //    ex2.approx per score, masks only on steps that cross a row's position,
-//    tree reductions for the row max and sum.  The running max
-//    is only moved -- and O in TMEM rescaled -- when a row's max grows by more
-//    than 2^8; between moves P may exceed 1 (at most 256), which fp16/bf16
-//    carry exactly as far as their precision goes, and numerator and
-//    denominator share the same reference.  In the last step they zero V rows
-//    past the keys in use, so tail slots (whatever they hold) cannot reach O.
-//  * warp 4, one thread: issues S = Q K^T (M 128, N = KEYS, K 128: 8 MMAs)
-//    into one of two TMEM score buffers and O += P V (M 128, N 128, K = KEYS,
-//    V as an MN-major operand) into the TMEM output, committing each to an
-//    mbarrier.  S for step j+1 is issued before P V of step j, so the tensor
-//    core works while the softmax warps do.
+//    tree reductions for the row max and sum.  The running max is only moved
+//    -- and O in TMEM rescaled -- when a row's max grows by more than 2^8;
+//    between moves P may exceed 1 (at most 256), which fp16/bf16 carry exactly
+//    as far as their precision goes, and numerator and denominator share the
+//    same reference.  In the last step they zero V rows past the keys in use,
+//    so tail slots (whatever they hold) cannot reach O.
+//  * warp 4, one thread: issues S = Q K^T (M 128, N KEYS, K 128: 8 MMAs, Q
+//    from TMEM) into one of two TMEM score buffers and O += P V (M 128, N 128,
+//    K KEYS, P from TMEM, V an MN-major shared-memory operand), committing each
+//    to an mbarrier.  S for step j+1 is in flight while the softmax warps work
+//    on step j; S for step j+2 reuses step j's buffer once P V of step j (which
+//    reads P there) has completed.
 //  * warp 5, one thread: stages KEYS-key K/V steps (16-row sub-tiles, two
 //    128-byte boxes each for K and V) through the block table with 2-D TMA into
 //    a ring of S stages, refilling a stage once the P V product that read it
 //    has completed.
-// KEYS = 32 and S = 3 keep a CTA under half of the SM's shared memory, so two
-// CTAs run per SM (measured 694 vs 526 TFLOP/s for one CTA with 64-key steps).
-// TMEM: scores in columns 0..2 KEYS (two buffers), O in columns 128-255.
-// bf16 carries P as hi + lo parts (two P V MMAs), so P keeps ~16 bits.
+// TMEM (KEYS = 32: 256 columns, so two CTAs share an SM): scores/P in columns
+// 0..2 KEYS, Q in the next 64 (two 16-bit values per column), O in 128-255.
+// bf16 carries P as hi + lo parts (two P V MMAs), so P keeps ~16 bits; the lo
+// part sits in the second half of the score buffer.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,28 +53,64 @@ namespace {
 
 constexpr int kTcRows = 128;     // query rows per CTA = TMEM lanes
 constexpr int kTcDim = 128;      // head_dim
-constexpr int kAtomRows128 = kTcRows * 128;  // one 64-dim atom of 128 rows (bytes)
 constexpr float kRescaleLog2 = 8.f;         // move the running max only past this growth
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// D (TMEM) [+]= A (TMEM, K-major: lane = row, column c = elements 2c, 2c+1) * B (smem)
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Where each operand lives.  32-key steps keep Q in TMEM (64 columns next to
+// two 32-column score buffers and O); 64-key steps need 128 columns of score
+// buffers, so Q is read from shared memory (128-byte swizzled, K-major).  Both
+// fit 256 columns, so two CTAs share an SM.
+template <int KEYS>
+struct TcLayout {
+  static constexpr bool kQInTmem = KEYS == 32;
+  static constexpr int kSCol = 0;                          // score buffers: [2][KEYS]
+  static constexpr int kQCol = 2 * KEYS;                   // Q in TMEM: 64 columns
+  static constexpr int kOCol = 128;                        // O: 128 columns
+  static constexpr int kCols = 256;
+  static constexpr int kAtomRows64 = KEYS * 128;           // one 64-dim atom of a step (bytes)
+  static constexpr int kAtomRows128 = kTcRows * 128;       // one 64-dim atom of Q (bytes)
+  static constexpr int kQBytes = kQInTmem ? 0 : 2 * kAtomRows128;
+  static constexpr int kStageBytes = 4 * kAtomRows64;      // K: 2 atoms, V: 2 atoms
+  static_assert(KEYS == 32 || KEYS == 64, "32- or 64-key steps");
+  static_assert(!kQInTmem || kQCol + 64 <= kOCol, "Q overlaps O");
+  static_assert(2 * KEYS <= kOCol, "scores overlap O");
+};
+
 template <typename T, int S, bool SPLIT, int KEYS>
-__global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
+__global__ void __launch_bounds__(192, 2)
     pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  using L = TcLayout<KEYS>;
   constexpr int kTcKeys = KEYS;                 // keys per step
-  constexpr int kAtomRows64 = kTcKeys * 128;    // one 64-dim atom of the step's key rows (bytes)
+  constexpr int kAtomRows64 = L::kAtomRows64;
   constexpr int kSub = kTcKeys / 16;            // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
-  // P rows have a 128-byte pitch; with 32-key steps the lo parts use the second
-  // half of each row (byte offset 64), otherwise a second tile
-  constexpr bool kLoInline = SPLIT && KEYS == 32;
-  constexpr int kQOff = 0;                                   // 2 atoms x 128 rows
-  constexpr int kPOff = 2 * kAtomRows128;                    // P hi: 128 rows x KEYS keys
-  constexpr int kPLoOff = kPOff + kAtomRows128;              // P lo, own tile (KEYS == 64)
-  constexpr int kStageOff = kPOff + (SPLIT && !kLoInline ? 2 : 1) * kAtomRows128;
-  constexpr int kStageBytes = 4 * kAtomRows64;               // K: 2 atoms, V: 2 atoms
+  constexpr int kStageBytes = L::kStageBytes;
+  constexpr int kStageOff = L::kQBytes;
   constexpr int kBarOff = kStageOff + S * kStageBytes;
+  constexpr int kPCols = kTcKeys / 2;           // P of one step: two 16-bit values per column
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+  static_assert(!SPLIT || 2 * kPCols <= kTcKeys, "P hi + lo must fit the score buffer");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -100,7 +141,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
     mbar_init(q_ready, kTcRows);
     fence_barrier_init();
   }
-  if (warp == 4) tmem_alloc(tmem_slot, 256);
+  if (warp == 4) tmem_alloc(tmem_slot, L::kCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -129,26 +170,46 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
     const int tok = t_first + r / G;
     const bool row_ok = r < tpc * G && tok <= t_last;
     const int pos = base_pos + tok;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     {
       const T *qrow = static_cast<const T *>(a.query) +
                       (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
                        r % G) * kTcDim;
+      if constexpr (L::kQInTmem) {
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
-                               : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(smem + kQOff + (ch >> 3) * kAtomRows128 + r * 128 +
-                                   (((ch & 7) ^ (r & 7)) << 4)) = v;
+        for (int part = 0; part < 4; ++part) {
+          uint32_t qv[16];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + part * 32 + ch * 8)
+                                   : make_uint4(0, 0, 0, 0);
+            qv[4 * ch] = v.x;
+            qv[4 * ch + 1] = v.y;
+            qv[4 * ch + 2] = v.z;
+            qv[4 * ch + 3] = v.w;
+          }
+          tmem_st16(lane_addr + L::kQCol + part * 16, qv);
+        }
+        tmem_wait_st();
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
+                                 : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * L::kAtomRows128 + r * 128 +
+                                     (((ch & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
       }
     }
-    fence_proxy_async_smem();
+    tc_fence_before();
     mbar_arrive(q_ready);
 
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_ref = -INFINITY, l = 0.f;
     bool ok_run = true;
     for (int j = 0; j < n_steps && ok_run; ++j) {
       const int s = j % S;
+      const uint32_t sbuf = lane_addr + L::kSCol + (j & 1) * kTcKeys;
       // warp-uniform decisions: the TMEM loads and stores below are warp-collective
       const bool got = mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1) &&
                        mbar_wait_bounded(&kv_full[s], (j / S) & 1);
@@ -162,7 +223,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
 #pragma unroll
       for (int q = 0; q < kTcKeys / 32; ++q) {
         float t0[32];
-        tmem_ld32(lane_addr + (j & 1) * kTcKeys + 32 * q, t0);
+        tmem_ld32(sbuf + 32 * q, t0);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
@@ -170,6 +231,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
       const int key0 = j * kTcKeys;
       const uint32_t vmask = step_valid[s];
       // zero V rows this step must not use: past the keys in use, or never loaded
+      bool zeroed = false;
       if (key0 + kTcKeys > n_keys || vmask != kAllSub) {
         const int kr = r >> 1, atom = r & 1;
         if (kr < kTcKeys && (key0 + kr >= n_keys || !((vmask >> (kr >> 4)) & 1u))) {
@@ -178,6 +240,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
 #pragma unroll
           for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
         }
+        zeroed = true;
       }
       // mask (only steps that reach past the row's position or hold an
       // unloaded sub-tile need it) and the row max of the raw scores
@@ -190,7 +253,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
           sv[c] = ok ? sv[c] : -INFINITY;
         }
       }
-      constexpr int kCh = kTcKeys / 8;  // 8-score chunks (16 bytes of P each)
+      constexpr int kCh = kTcKeys / 8;  // 8-score chunks
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
@@ -211,10 +274,9 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
         m_ref = m_new;
       }
       // P = 2^(s scale - m): one FFMA and one ex2 per score; a row with no key
-      // yet (m = -inf) gets 2^-inf = 0 everywhere.  Packed in registers first,
-      // so the previous P V product has time to finish.
+      // yet (m = -inf) gets 2^-inf = 0 everywhere
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t ph[kCh * 4], pl[SPLIT ? kCh * 4 : 1];
+      uint32_t ph[kPCols], pl[SPLIT ? kPCols : 1];
       float ls[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls[i] = 0.f;
@@ -234,38 +296,37 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
         }
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // P V of the previous step read P and wrote O: wait for it before touching either
-      if (j > 0 && !__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
-        if (lane == 0) atomicOr(a.err, kErrTimeout);
-        ok_run = false;
-        break;
+      // P over the scores it came from: the buffer is this step's alone (step
+      // j-2's P V completed before S of step j was issued into it)
+#pragma unroll
+      for (int c = 0; c < kPCols; c += 16) {
+        tmem_st16(sbuf + c, ph + c);
+        if constexpr (SPLIT) tmem_st16(sbuf + kPCols + c, pl + c);
       }
-      tc_fence_after();
-      if (j > 0 && __any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
+      // P V of the previous step: waited for every step, so this warp is never
+      // more than one phase of pv_done behind (a parity wait cannot tell phase
+      // k from k + 2) and O holds every earlier product before it is rescaled
+      if (j > 0) {
+        if (!__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
+          if (lane == 0) atomicOr(a.err, kErrTimeout);
+          ok_run = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float o[32];
-          tmem_ld32(lane_addr + 128 + cb * 32, o);
-          tmem_wait_ld();
+          for (int cb = 0; cb < 4; ++cb) {
+            float o[32];
+            tmem_ld32(lane_addr + L::kOCol + cb * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(lane_addr + 128 + cb * 32, o);
-        }
-        tmem_wait_st();
-      }
-#pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) {
-        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4 *>(smem + kPOff + off) =
-            make_uint4(ph[ch * 4], ph[ch * 4 + 1], ph[ch * 4 + 2], ph[ch * 4 + 3]);
-        if constexpr (SPLIT) {
-          const int lo_off = kLoInline ? kPOff + r * 128 + (((ch + 4) ^ (r & 7)) << 4)
-                                       : kPLoOff + off;
-          *reinterpret_cast<uint4 *>(smem + lo_off) =
-              make_uint4(pl[ch * 4], pl[ch * 4 + 1], pl[ch * 4 + 2], pl[ch * 4 + 3]);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_addr + L::kOCol + cb * 32, o);
+          }
         }
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      if (zeroed) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
     }
@@ -279,7 +340,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float o[32];
-          tmem_ld32(lane_addr + 128 + cb * 32, o);
+          tmem_ld32(lane_addr + L::kOCol + cb * 32, o);
           tmem_wait_ld();
           if (row_ok) {
 #pragma unroll
@@ -302,10 +363,9 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
     if (lane == 0) {
       const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kTcKeys);
       const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
-      const uint32_t sq = smem_addr(smem + kQOff), sp = smem_addr(smem + kPOff);
-      const uint32_t splo = smem_addr(smem + kPLoOff);
-      const uint32_t sst = smem_addr(smem + kStageOff);
+      const uint32_t sst = smem_addr(smem + kStageOff), sq = smem_addr(smem);
       bool ok_run = mbar_wait_bounded(q_ready, 0);
+      if (ok_run) tc_fence_after();
       auto issue_qk = [&](int j) -> bool {
         const int s = j % S;
         if (!mbar_wait_bounded(&kv_full[s], (j / S) & 1)) return false;
@@ -313,41 +373,55 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
         const uint32_t kb = sst + s * kStageBytes;
 #pragma unroll
         for (int k = 0; k < kTcDim / 16; ++k) {
-          const uint64_t da = umma_desc_sw128(sq + (k >> 2) * kAtomRows128 + (k & 3) * 32, 16, 1024);
           const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kAtomRows64 + (k & 3) * 32, 16, 1024);
-          umma_f16(tmem + (j & 1) * kTcKeys, da, db, id_qk, k > 0);
+          if constexpr (L::kQInTmem) {
+            umma_f16_ts(tmem + L::kSCol + (j & 1) * kTcKeys, tmem + L::kQCol + k * 8, db, id_qk,
+                        k > 0);
+          } else {
+            const uint64_t da =
+                umma_desc_sw128(sq + (k >> 2) * L::kAtomRows128 + (k & 3) * 32, 16, 1024);
+            umma_f16(tmem + L::kSCol + (j & 1) * kTcKeys, da, db, id_qk, k > 0);
+          }
         }
         umma_commit(&s_full[j & 1]);
         return true;
       };
       if (ok_run) ok_run = issue_qk(0);
+      if (ok_run && n_steps > 1) ok_run = issue_qk(1);
       for (int j = 0; j < n_steps && ok_run; ++j) {
-        if (j + 1 < n_steps && !issue_qk(j + 1)) {
-          ok_run = false;
-          break;
-        }
         if (!mbar_wait_bounded(p_full, j & 1)) {
           ok_run = false;
           break;
         }
         tc_fence_after();
         const uint32_t vb = sst + (j % S) * kStageBytes + 2 * kAtomRows64;
+        const uint32_t pa_col = tmem + L::kSCol + (j & 1) * kTcKeys;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint64_t da = umma_desc_sw128(sp + kk * 32, 16, 1024);
           const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
-          umma_f16(tmem + 128, da, dv, id_pv, j > 0 || kk > 0);
+          umma_f16_ts(tmem + L::kOCol, pa_col + kk * 8, dv, id_pv, j > 0 || kk > 0);
         }
         if constexpr (SPLIT) {
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint64_t da = umma_desc_sw128((kLoInline ? sp + 64 : splo) + kk * 32, 16, 1024);
             const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
-            umma_f16(tmem + 128, da, dv, id_pv, true);
+            umma_f16_ts(tmem + L::kOCol, pa_col + kPCols + kk * 8, dv, id_pv, true);
           }
         }
         umma_commit(pv_done);
         umma_commit(&kv_empty[j % S]);
+        // S of step j+2 goes where P of step j is: wait for this P V to finish
+        if (j + 2 < n_steps) {
+          if (!mbar_wait_bounded(pv_done, j & 1)) {
+            ok_run = false;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_qk(j + 2)) {
+            ok_run = false;
+            break;
+          }
+        }
       }
       if (!ok_run) atomicOr(a.err, kErrTimeout);
     }
@@ -422,7 +496,7 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
   __syncthreads();
   if (warp == 4) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, L::kCols);
   }
   grid_launch_dependents();
 }
@@ -430,9 +504,9 @@ __global__ void __launch_bounds__(192, KEYS == 32 ? 2 : 1)
 template <typename T, int S, bool SPLIT, int KEYS>
 cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                                 cudaStream_t stream) {
-  constexpr size_t smem = 1024 + 2 * kAtomRows128 +
-                          (SPLIT && KEYS != 32 ? 2 : 1) * kAtomRows128 +
-                          static_cast<size_t>(S) * 4 * KEYS * 128 + (2 * S + 5) * 8 + 8 + S * 4;
+  constexpr size_t smem = 1024 + TcLayout<KEYS>::kQBytes +
+                          static_cast<size_t>(S) * TcLayout<KEYS>::kStageBytes +
+                          (2 * S + 5) * 8 + 8 + S * 4;
   auto kern = pa_prefill_tc_kernel<T, S, SPLIT, KEYS>;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -453,10 +527,10 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 
 }  // namespace
 
-// 32-key steps x 3 stages keep a CTA under half the shared memory, so two
-// CTAs (two softmax warps per scheduler, two MMA streams) share an SM.
+// 32-key steps take 256 TMEM columns, so two CTAs (two softmax warps per
+// scheduler, two MMA streams) share an SM; each holds a ring of 16 KB K/V stages.
 #ifndef PA_PREFILL_TC_STAGES
-#define PA_PREFILL_TC_STAGES 3
+#define PA_PREFILL_TC_STAGES 6
 #endif
 #ifndef PA_PREFILL_TC_KEYS
 #define PA_PREFILL_TC_KEYS 32

@@ -88,3 +88,37 @@ def test_prefill_bad_length_flagged(pa):
     assert err & pa.DEVERR_BAD_LEN
     q0 = int(pw.query_start[0])
     assert torch.isfinite(out[q0:q0 + 10].float()).all()
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_prefill_bench_size_repeatable(pa, dtype):
+    """The batch the prefill bench times (64 sequences, 512-token chunks):
+    three back-to-back launches give bit-identical outputs (the products run
+    in a fixed order, so any difference is a race), and four whole sequences
+    of the first match the oracle."""
+    pw = W.make_prefill("llama3_8b_gqa", 64, chunk=512, dtype=dtype)
+    dev = torch.device("cuda")
+    kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
+    pa.pa_reshape_and_cache(pw.key.to(dev), pw.value.to(dev), kc, vc, pw.slot_mapping.to(dev))
+    q, qs = pw.query.to(dev), pw.query_start.to(dev)
+    bt, cl = pw.block_tables.to(dev), pw.context_lens.to(dev)
+    outs = []
+    for _ in range(3):
+        out = torch.full_like(q, float("nan"))
+        pa.pa_prefill(out, q, qs, kc, vc, bt, cl, pw.scale, pw.max_q_len)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    # the oracle on four whole sequences of the launch (each sequence is independent)
+    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
+    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    qs_h = pw.query_start.numpy()
+    for i in (0, 21, 42, 63):
+        a, b = int(qs_h[i]), int(qs_h[i + 1])
+        ref = oracle.prefill(pw.query[a:b], np.array([0, b - a], dtype=np.int32), kh, vh,
+                             pw.block_tables[i:i + 1], pw.context_lens[i:i + 1], pw.scale, pw.dtype)
+        got = outs[0][a:b].float().cpu().double().numpy()
+        err = np.abs(got - ref)
+        assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
