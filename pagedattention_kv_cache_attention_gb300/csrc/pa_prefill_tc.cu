@@ -80,6 +80,34 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
 // two 32-column score buffers and O); 64-key steps need 128 columns of score
 // buffers, so Q is read from shared memory (128-byte swizzled, K-major).  Both
 // fit 256 columns, so two CTAs share an SM.
+// Packed fp32 pairs (sm_100 and later): two IEEE fp32 operations per instruction,
+// each rounded exactly as the scalar one.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int KEYS>
 struct TcLayout {
   static constexpr bool kQInTmem = KEYS == 32;
@@ -525,6 +553,522 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
                           km, vm, a);
 }
 
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA, 64-key steps, scores double-buffered per tile.
+//
+// One CTA per SM holds two 128-row tiles of the same (sequence, KV head) --
+// 256 rows = 256/G tokens x G heads -- and streams 64-key K/V steps through
+// two rings shared by both tiles (K and V apart, so a K stage is refilled as
+// soon as the Q K^T products that read it are done).  Each tile owns 256 TMEM
+// columns: two 64-column score buffers and O (128); P is written over the
+// scores it came from.  While a tile's softmax warps work on step n, the
+// tensor core already computes that tile's scores of step n + 1 and the other
+// tile's products, so both tiles' softmax warps can be busy at once and the
+// tensor core is fed from two independent streams.  Q is read from shared
+// memory (two 32 KB tiles).
+// Warp roles: warps 0-3 softmax for tile 0, 4-7 for tile 1 (thread r of a
+// tile owns its row r and TMEM lane r), warps 8 and 9 issue the MMAs of tile
+// 0 and tile 1, warp 10 runs the TMA producer.  One thread issuing
+// tcgen05.mma back to back gets about one instruction per 120 cycles whatever
+// N is (measured on GB300), so each tile has its own issuing warp; the two
+// streams overlap on the tensor core.  V rows a product must not use (past the keys in use, or
+// in a sub-tile whose block id is out of range) are zeroed by the producer
+// before the stage is handed over; the softmax warps mask those keys.
+constexpr int kPairKeys = 64;                  // keys per step
+constexpr int kPairThreads = 352;              // 11 warps
+constexpr int kPairQAtom = kTcRows * 128;      // one 64-dim atom of a Q tile (bytes)
+constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V stage (bytes)
+
+template <int SK, int SV>
+struct PairLayout {
+  static constexpr int kQOff = 0;                              // Q: [2 tiles][2 atoms]
+  static constexpr int kKOff = 4 * kPairQAtom;                 // K ring: [SK][2 atoms]
+  static constexpr int kVOff = kKOff + SK * 2 * kPairKvAtom;   // V ring: [SV][2 atoms]
+  static constexpr int kBarOff = kVOff + SV * 2 * kPairKvAtom;
+  static constexpr int kBars = 2 * SK + 2 * SV + 1 + 4 + 2 + 2 + 1;
+  static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
+};
+
+template <typename T, int SK, int SV, bool SPLIT>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
+                              const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  using L = PairLayout<SK, SV>;
+  constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
+  constexpr uint32_t kAllSub = (1u << kSub) - 1;
+  constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+  uint64_t *k_empty = k_full + SK;
+  uint64_t *v_full = k_empty + SK;
+  uint64_t *v_empty = v_full + SV;
+  uint64_t *v_tail = v_empty + SV;     // the last step's V load, before its tail is zeroed
+  uint64_t *s_full = v_tail + 1;       // [2 tiles][2 buffers]
+  uint64_t *p_full = s_full + 4;       // [2 tiles]
+  uint64_t *pv_done = p_full + 2;      // [2 tiles]
+  uint64_t *q_ready = pv_done + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
+
+  const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.group;
+  const int tpc = 2 * kTcRows / G;     // tokens per CTA
+
+  if (tid == 0) {
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 2);  // released by both issuers
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 2);
+    }
+    mbar_init(v_tail, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&s_full[i], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&p_full[t], kTcRows);
+      mbar_init(&pv_done[t], 1);
+    }
+    mbar_init(q_ready, 2 * kTcRows);
+    fence_barrier_init();
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dependency_wait();  // the chunk's K/V may come from the kernel before
+
+  const int q0 = a.query_start[seq];
+  const int q_len = a.query_start[seq + 1] - q0;
+  const int ctx = a.context_lens[seq];
+  bool active = true;
+  if (q_len < 0 || ctx < q_len || ctx > (a.max_blocks_per_seq << a.bs_log2) ||
+      q_len > a.max_q_len) {
+    if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
+    active = false;
+  }
+  const int t_first = tile * tpc;
+  if (t_first >= q_len) active = false;
+  const int t_last = min(q_len, t_first + tpc) - 1;
+  const int base_pos = ctx - q_len;
+  // per tile: last token (-1 when the tile has no rows) and step count; tile 1
+  // holds the later tokens, so it reads every step tile 0 reads
+  const int half = kTcRows / G;
+  const int last0 = min(t_last, t_first + half - 1);
+  const int last1 = t_first + half <= t_last ? t_last : -1;
+  const int n_keys = base_pos + t_last + 1;
+  const int n_steps0 = active ? (base_pos + last0 + 1 + kPairKeys - 1) / kPairKeys : 0;
+  const int n_steps1 = active && last1 >= 0 ? (n_keys + kPairKeys - 1) / kPairKeys : 0;
+  const int n_steps = max(n_steps0, n_steps1);
+  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
+  const int n_sub = (n_keys + 15) / 16;
+
+  if (active && warp < 8) {
+    // ------------------------------------------------------------ softmax warps
+    const int t = warp >> 2;
+    const int r = tid & (kTcRows - 1);                 // row within the tile = TMEM lane
+    const int rc = t * kTcRows + r;                    // row within the CTA
+    const int tok = t_first + rc / G;
+    const bool row_ok = tok <= t_last;
+    const int pos = base_pos + tok;
+    const int my_steps = t == 0 ? n_steps0 : n_steps1;
+    {
+      const T *qrow = static_cast<const T *>(a.query) +
+                      (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
+                       rc % G) * kTcDim;
+      uint8_t *qt = smem + L::kQOff + t * 2 * kPairQAtom;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
+                               : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(qt + (ch >> 3) * kPairQAtom + r * 128 +
+                                   (((ch & 7) ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+    }
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + t * 256;
+    // sub-tile validity, as the producer decides it (lane h < kSub: sub-tile h of a step)
+    auto step_mask = [&](int n) -> uint32_t {
+      const int u = n * kSub + lane;
+      bool ok = false;
+      if (lane < kSub && u < n_sub) {
+        const int phys = bt_row[(u * 16) >> a.bs_log2];
+        ok = phys >= 0 && static_cast<int64_t>(phys) < a.num_blocks;
+      }
+      return __ballot_sync(kFullMask, ok) & kAllSub;
+    };
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok_run = true;
+    uint32_t vmask_next = my_steps > 0 ? step_mask(0) : 0;
+    for (int n = 0; n < my_steps && ok_run; ++n) {
+      const uint32_t vmask = vmask_next;
+      const uint32_t sbuf = lane_addr + (n & 1) * kPairKeys;
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&s_full[2 * t + (n & 1)], (n >> 1) & 1))) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        ok_run = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[kPairKeys];
+#pragma unroll
+      for (int q = 0; q < kPairKeys / 32; ++q) {
+        float t0[32];
+        tmem_ld32(sbuf + 32 * q, t0);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
+      }
+      if (n + 1 < my_steps) vmask_next = step_mask(n + 1);  // overlaps the softmax below
+      const int key0 = n * kPairKeys;
+      const bool full_step = row_ok && key0 + kPairKeys - 1 <= pos && vmask == kAllSub;
+      if (!full_step) {
+#pragma unroll
+        for (int c = 0; c < kPairKeys; ++c) {
+          const int key = key0 + c;
+          const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
+          sv[c] = ok ? sv[c] : -INFINITY;
+        }
+      }
+      // row max: three-input max, 64 -> 22 -> 8 -> 3 -> 1
+      static_assert(kPairKeys == 64, "max tree written for 64 keys");
+      float t22[22], t8[8];
+#pragma unroll
+      for (int j = 0; j < 21; ++j) t22[j] = fmax3(sv[3 * j], sv[3 * j + 1], sv[3 * j + 2]);
+      t22[21] = sv[63];
+#pragma unroll
+      for (int j = 0; j < 7; ++j) t8[j] = fmax3(t22[3 * j], t22[3 * j + 1], t22[3 * j + 2]);
+      t8[7] = t22[21];
+      const float tmax_raw = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
+                                   fmaxf(t8[6], t8[7]));
+      const float tmax = tmax_raw * a.scale_log2;  // the scale is positive: same order
+      const float m_new = fmaxf(m_ref, tmax);
+      const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
+      const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - m_new));
+      if (move) {
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      // P in 32-key chunks, each stored as soon as it is packed.  fp16: chunk c
+      // in columns 16c..16c+15 of the buffer (key k in column k/2).  bf16: hi
+      // and lo parts of chunk c in columns 32c..32c+15 and 32c+16..32c+31.
+      // Either way a chunk only overwrites scores this thread has already read.
+      // s scale - m and the row sum run on packed fp32 pairs.
+      const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t negm2 = f2_pack(neg_m, neg_m);
+      uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
+#pragma unroll
+      for (int c = 0; c < kPairKeys / 32; ++c) {
+        uint32_t ph[16], pl[SPLIT ? 16 : 1];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]),
+                                            scale2, negm2));
+          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
+          ph[e] = Elem<T>::pack(p0, p1);
+          if constexpr (SPLIT) {
+            const float2 h = Elem<T>::unpack(ph[e]);
+            pl[e] = Elem<T>::pack(p0 - h.x, p1 - h.y);
+          }
+        }
+        if constexpr (SPLIT) {
+          tmem_st16(sbuf + 32 * c, ph);
+          tmem_st16(sbuf + 32 * c + 16, pl);
+        } else {
+          tmem_st16(sbuf + 16 * c, ph);
+        }
+      }
+      {
+        const float2 s = f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])));
+        l += s.x + s.y;
+      }
+      // P V of the previous step: waited for every step, so this warp is never
+      // more than one phase of pv_done behind (a parity wait cannot tell phase
+      // k from k + 2) and O holds every earlier product before it is rescaled
+      if (n > 0) {
+        if (!__all_sync(kFullMask, mbar_wait_bounded(&pv_done[t], (n - 1) & 1))) {
+          if (lane == 0) atomicOr(a.err, kErrTimeout);
+          ok_run = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            float o[32];
+            tmem_ld32(lane_addr + 128 + cb * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_addr + 128 + cb * 32, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    // ---- epilogue: O / l for this row
+    if (ok_run && my_steps > 0) {
+      if (__all_sync(kFullMask, mbar_wait_bounded(&pv_done[t], (my_steps - 1) & 1))) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T *orow = static_cast<T *>(a.out) +
+                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G) * kTcDim;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float o[32];
+          tmem_ld32(lane_addr + 128 + cb * 32, o);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 pk;
+              pk.x = Elem<T>::pack(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              pk.y = Elem<T>::pack(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              pk.z = Elem<T>::pack(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              pk.w = Elem<T>::pack(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              *reinterpret_cast<uint4 *>(orow + cb * 32 + q * 8) = pk;
+            }
+          }
+        }
+      } else if (lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+      }
+    }
+  } else if (active && (warp == 8 || warp == 9)) {
+    // ------------------------------------------------------- MMA issuer (tile)
+    // Per step n: Q K^T of step n + 1 (into the buffer P V of step n - 1
+    // read, so that product must be complete), then P V of step n once its P
+    // is in place.  The scores of step n + 1 are thus computed while the
+    // softmax warps work on step n.  Each issuer releases every K and V stage
+    // once (count-2 barriers); for steps its tile does not read it waits for
+    // the stage to fill first, so its release lands in that step's phase.
+    if (lane == 0) {
+      const int t = warp - 8;
+      const int nt = t == 0 ? n_steps0 : n_steps1;
+      const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
+      const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
+      const uint32_t qb = smem_addr(smem + L::kQOff) + t * 2 * kPairQAtom;
+      const uint32_t sk0 = smem_addr(smem + L::kKOff), sv0 = smem_addr(smem + L::kVOff);
+      const uint32_t tt = tmem + t * 256;
+      auto issue_qk = [&](int n) {
+        const uint32_t kb = sk0 + (n % SK) * 2 * kPairKvAtom;
+#pragma unroll
+        for (int k = 0; k < kTcDim / 16; ++k) {
+          const uint64_t da = umma_desc_sw128(qb + (k >> 2) * kPairQAtom + (k & 3) * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kPairKvAtom + (k & 3) * 32, 16, 1024);
+          umma_f16(tt + (n & 1) * kPairKeys, da, db, id_qk, k > 0);
+        }
+        umma_commit(&s_full[2 * t + (n & 1)]);
+        umma_commit(&k_empty[n % SK]);
+      };
+      bool ok_run = mbar_wait_bounded(q_ready, 0);
+      if (ok_run && nt > 0) {
+        ok_run = mbar_wait_bounded(&k_full[0], 0);
+        if (ok_run) {
+          tc_fence_after();
+          issue_qk(0);
+        }
+      }
+      for (int n = 0; n < nt && ok_run; ++n) {
+        if (n + 1 < nt) {
+          if ((n > 0 && !mbar_wait_bounded(&pv_done[t], (n - 1) & 1)) ||
+              !mbar_wait_bounded(&k_full[(n + 1) % SK], ((n + 1) / SK) & 1)) {
+            ok_run = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(n + 1);
+        }
+        const int s = n % SV;
+        if (!mbar_wait_bounded(&p_full[t], n & 1) || !mbar_wait_bounded(&v_full[s], (n / SV) & 1)) {
+          ok_run = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = sv0 + s * 2 * kPairKvAtom;
+        const uint32_t pcol = tt + (n & 1) * kPairKeys;
+#pragma unroll
+        for (int kk = 0; kk < kPairKeys / 16; ++kk) {
+          const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kPairKvAtom, 1024);
+          if constexpr (SPLIT) {
+            const uint32_t hi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
+            umma_f16_ts(tt + 128, hi, dv, id_pv, n > 0 || kk > 0);
+            umma_f16_ts(tt + 128, hi + 16, dv, id_pv, true);
+          } else {
+            umma_f16_ts(tt + 128, pcol + 8 * kk, dv, id_pv, n > 0 || kk > 0);
+          }
+        }
+        umma_commit(&pv_done[t]);
+        umma_commit(&v_empty[s]);
+      }
+      // stages of the steps this tile does not read
+      for (int m = nt; m < n_steps && ok_run; ++m) {
+        if (!mbar_wait_bounded(&k_full[m % SK], (m / SK) & 1)) {
+          ok_run = false;
+          break;
+        }
+        mbar_arrive(&k_empty[m % SK]);
+        if (!mbar_wait_bounded(&v_full[m % SV], (m / SV) & 1)) {
+          ok_run = false;
+          break;
+        }
+        mbar_arrive(&v_empty[m % SV]);
+      }
+      if (!ok_run) atomicOr(a.err, kErrTimeout);
+    }
+  } else if (active && warp == 10) {
+    // ---------------------------------------------------------- TMA producer
+    const int bs_mask = (1 << a.bs_log2) - 1;
+    auto block_of = [&](int u) -> int {
+      if (u >= n_sub) return -1;
+      const int phys = bt_row[(u * 16) >> a.bs_log2];
+      if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
+        atomicOr(a.err, kErrBadBlock);
+        return -1;
+      }
+      return phys;
+    };
+    const uint64_t policy = l2_policy_evict_first();
+    int win_base = 0;
+    int win = block_of(lane);
+    bool ok_run = true;
+    for (int n = 0; n < n_steps && ok_run; ++n) {
+      if (n * kSub >= win_base + 32) {
+        win_base += 32;
+        win = block_of(win_base + lane);
+      }
+      int phys[kSub];
+      uint32_t mask = 0;
+#pragma unroll
+      for (int h = 0; h < kSub; ++h) {
+        phys[h] = __shfl_sync(kFullMask, win, n * kSub + h - win_base);
+        if (phys[h] >= 0) mask |= 1u << h;
+      }
+      const uint32_t bytes = __popc(mask) * 2 * 2048;
+      auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
+#pragma unroll
+        for (int h = 0; h < kSub; ++h) {
+          if (phys[h] < 0) continue;
+          const int u = n * kSub + h;
+          const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+            tma_load_2d(st + b * kPairKvAtom + h * 2048, map, b * 64, y, bar, policy);
+        }
+      };
+      // K
+      const int sk = n % SK;
+      if (lane == 0) {
+        if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
+          ok_run = false;
+        } else if (bytes == 0) {
+          mbar_arrive(&k_full[sk]);
+        } else {
+          mbar_arrive_expect_tx(&k_full[sk], bytes);
+          load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
+        }
+      }
+      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+      if (!ok_run) break;
+      // V: rows past the keys in use and sub-tiles not loaded become zeros
+      const int sv = n % SV;
+      uint8_t *vst = smem + L::kVOff + sv * 2 * kPairKvAtom;
+      if (lane == 0 && n >= SV && !mbar_wait_bounded(&v_empty[sv], ((n / SV) - 1) & 1))
+        ok_run = false;
+      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+      if (!ok_run) break;
+      const int key0 = n * kPairKeys;
+      const bool tail = key0 + kPairKeys > n_keys;
+      if (mask != kAllSub) {
+        // sub-tiles with no load: zero both 64-dim atoms of their 16 rows
+        for (int i = lane; i < kSub * 2 * 16 * 8; i += 32) {  // 16-byte units
+          const int h = i >> 8, b = (i >> 7) & 1, row = (i >> 3) & 15, u16 = i & 7;
+          if (!((mask >> h) & 1u))
+            *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + (h * 16 + row) * 128 + u16 * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!tail) {
+        if (lane == 0) {
+          if (bytes == 0) {
+            mbar_arrive(&v_full[sv]);
+          } else {
+            mbar_arrive_expect_tx(&v_full[sv], bytes);
+            load(vst, &vmap, &v_full[sv]);
+          }
+        }
+      } else {
+        // the last step: load, wait, zero the rows past n_keys, then hand over
+        bool got = true;
+        if (lane == 0 && bytes > 0) {
+          mbar_arrive_expect_tx(v_tail, bytes);
+          load(vst, &vmap, v_tail);
+          got = mbar_wait_bounded(v_tail, 0);
+        }
+        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          ok_run = false;
+          break;
+        }
+        const int first = n_keys - key0;  // first row to clear
+        for (int i = lane; i < kPairKeys * 2 * 8; i += 32) {
+          const int row = i >> 4, b = (i >> 3) & 1, u16 = i & 7;
+          if (row >= first)
+            *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + row * 128 + u16 * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v_full[sv]);
+      }
+    }
+    if (!ok_run && lane == 0) atomicOr(a.err, kErrTimeout);
+  }
+
+  // ---- teardown: every tcgen05 operation is complete once each tile's last
+  // pv_done phase has been observed by its softmax warps (or it had no work)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  grid_launch_dependents();
+}
+
+template <typename T, int SK, int SV, bool SPLIT>
+cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km,
+                                     const CUtensorMap &vm, cudaStream_t stream) {
+  constexpr size_t smem = PairLayout<SK, SV>::kSmem;
+  static_assert(smem <= 227 * 1024, "shared memory");
+  auto kern = pa_prefill_tc_pair_kernel<T, SK, SV, SPLIT>;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int tpc = 2 * kTcRows / a.group;
+  const int tiles = (a.max_q_len + tpc - 1) / tpc;
+  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(kPairThreads), smem,
+                          stream, km, vm, a);
+}
+
 }  // namespace
 
 // 32-key steps take 256 TMEM columns, so two CTAs (two softmax warps per
@@ -536,15 +1080,33 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 #define PA_PREFILL_TC_KEYS 32
 #endif
 
+#ifndef PA_PREFILL_PAIR_KSTAGES
+#define PA_PREFILL_PAIR_KSTAGES 4
+#endif
+#ifndef PA_PREFILL_PAIR_VSTAGES
+#define PA_PREFILL_PAIR_VSTAGES 4
+#endif
+
 bool prefill_tc_supported(int head_dim, int group) {
   return head_dim == kTcDim && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
+// Chunks that fill more than one 128-row tile go to the two-tile kernel; the
+// rest (short chunks, decode-like rows) to the 32-key kernel, which runs two
+// CTAs per SM.
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                               int dtype, cudaStream_t stream) {
-  if (dtype == 0)
+  const bool pair = static_cast<int64_t>(a.max_q_len) * a.group > kTcRows;
+  if (dtype == 0) {
+    if (pair)
+      return launch_prefill_tc_pair_t<__half, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
+                                      false>(a, km, vm, stream);
     return launch_prefill_tc_t<__half, PA_PREFILL_TC_STAGES, false, PA_PREFILL_TC_KEYS>(a, km, vm,
                                                                                       stream);
+  }
+  if (pair)
+    return launch_prefill_tc_pair_t<__nv_bfloat16, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
+                                    true>(a, km, vm, stream);
   return launch_prefill_tc_t<__nv_bfloat16, PA_PREFILL_TC_STAGES, true, PA_PREFILL_TC_KEYS>(a, km, vm,
                                                                                            stream);
 }
