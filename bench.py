@@ -191,8 +191,10 @@ def make_workload(args):
 
 def cpu_oracle_run(w, budget_s: float):
     """Time the oracle (scatter + fp64 decode) on a bounded sample: the first
-    n sequences, n grown until one run takes a good part of the budget.
-    Returns (GB/s, cores, sample description, seconds)."""
+    n sequences, n grown until one run takes a good part of the budget; when
+    the whole batch is quicker than that, the run is repeated until about two
+    thirds of the budget is spent.  Returns (GB/s, cores, sample description,
+    seconds, n)."""
     import numpy as np
     import torch
 
@@ -204,8 +206,8 @@ def cpu_oracle_run(w, budget_s: float):
         kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
         vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
     cores = oracle.max_threads()
-    n = min(w.num_seqs, 4)
-    while True:
+
+    def one_run(n):
         sub = slice(0, n)
         t0 = time.perf_counter()
         if fp8:
@@ -216,10 +218,18 @@ def cpu_oracle_run(w, budget_s: float):
         oracle.decode(w.query[sub], kh, vh, w.block_tables[sub], w.context_lens[sub], w.scale,
                       w.dtype, partition_size=w.partition_size,
                       kv_dtype="e4m3" if fp8 else None, k_scale=w.k_scale, v_scale=w.v_scale)
-        dt = time.perf_counter() - t0
+        return time.perf_counter() - t0
+
+    n = min(w.num_seqs, 4)
+    while True:
+        dt = one_run(n)
         if n >= w.num_seqs or dt > budget_s / 4:
             break
         n = min(w.num_seqs, max(n + 1, int(n * min(8.0, (budget_s / 3) / max(dt, 1e-3)))))
+    total, runs = dt, 1
+    while n >= w.num_seqs and total < budget_s * 2 / 3 and runs < 1000:
+        total += one_run(n)
+        runs += 1
     ctx = w.context_lens.numpy()[:n].astype(np.int64)
     s = w.elem_bytes
     byts = (2 * ctx.sum() * w.num_kv_heads * w.head_dim * s
@@ -227,8 +237,8 @@ def cpu_oracle_run(w, budget_s: float):
             + 4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * n
             + 2 * n * w.num_kv_heads * w.head_dim * (2 + s) + 8 * n)
     sample = (f"first {n} of {w.num_seqs} sequences of {w.name} (all {w.num_q_heads} query heads, "
-              f"{int(ctx.sum())} context tokens), scatter + fp64 decode, one run of {dt:.2f} s")
-    return byts / dt / 1e9, cores, sample, dt, n
+              f"{int(ctx.sum())} context tokens), scatter + fp64 decode, {runs} run(s) in {total:.2f} s")
+    return byts * runs / total / 1e9, cores, sample, total, n
 
 
 def run_reference(args):

@@ -122,3 +122,33 @@ def test_prefill_bench_size_repeatable(pa, dtype):
         got = outs[0][a:b].float().cpu().double().numpy()
         err = np.abs(got - ref)
         assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("chunk", [300, 20])   # two-tile kernel, one-tile kernel (G = 4)
+def test_prefill_bad_block_flagged_others_exact(pa, chunk):
+    """An out-of-range block id in one sequence's table: the call flags it,
+    reads nothing through it (that sequence's rows stay finite), and every
+    other sequence's rows still match the oracle."""
+    pw = W.make_prefill("llama3_8b_gqa", 65, lens=[700, 1400, 900], chunk=chunk)
+    dev = torch.device("cuda")
+    kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
+    pa.pa_reshape_and_cache(pw.key.to(dev), pw.value.to(dev), kc, vc, pw.slot_mapping.to(dev))
+    bt = pw.block_tables.clone()
+    bt[1, 5] = pw.num_blocks + 7          # a block well inside sequence 1's context
+    q, qs = pw.query.to(dev), pw.query_start.to(dev)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_prefill(out, q, qs, kc, vc, bt.to(dev), pw.context_lens.to(dev), pw.scale, pw.max_q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() & pa.DEVERR_BAD_BLOCK
+    qs_h = pw.query_start.numpy()
+    a1, b1 = int(qs_h[1]), int(qs_h[2])
+    assert torch.isfinite(out[a1:b1].float()).all()
+    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
+    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    for i in (0, 2):
+        a, b = int(qs_h[i]), int(qs_h[i + 1])
+        ref = oracle.prefill(pw.query[a:b], np.array([0, b - a], dtype=np.int32), kh, vh,
+                             pw.block_tables[i:i + 1], pw.context_lens[i:i + 1], pw.scale, pw.dtype)
+        got = out[a:b].float().cpu().double().numpy()
+        err = np.abs(got - ref)
+        assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
