@@ -477,44 +477,39 @@ __global__ void __launch_bounds__(192, 2)
         win_base += 32;
         win = block_of(win_base + lane);
       }
-      int phys[kSub];
-#pragma unroll
-      for (int h = 0; h < kSub; ++h) phys[h] = __shfl_sync(kFullMask, win, j * kSub + h - win_base);
+      // lane h < kSub issues the four copies of sub-tile h (one thread gets
+      // through a TMA copy every ~150 cycles)
+      const int my_phys = __shfl_sync(kFullMask, win, j * kSub + (lane & (kSub - 1)) - win_base);
+      const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
+      const uint32_t bytes = __popc(mask) * 4 * 2048;
       if (lane == 0) {
         if (j >= S && !mbar_wait_bounded(&kv_empty[s], ((j / S) - 1) & 1)) {
           atomicOr(a.err, kErrTimeout);
           ok_run = false;
         } else {
-          uint32_t mask = 0, bytes = 0;
-#pragma unroll
-          for (int h = 0; h < kSub; ++h)
-            if (phys[h] >= 0) {
-              mask |= 1u << h;
-              bytes += 4 * 2048;
-            }
           step_valid[s] = mask;
           if (bytes == 0) {
             mbar_arrive(&kv_full[s]);
           } else {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&kv_full[s], bytes);
-            uint8_t *st = smem + kStageOff + s * kStageBytes;
-#pragma unroll
-            for (int h = 0; h < kSub; ++h) {
-              if (phys[h] < 0) continue;
-              const int u = j * kSub + h;
-              const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                tma_load_2d(st + b * kAtomRows64 + h * 2048, &kmap, b * 64, y, &kv_full[s], policy);
-                tma_load_2d(st + (2 + b) * kAtomRows64 + h * 2048, &vmap, b * 64, y, &kv_full[s],
-                            policy);
-              }
-            }
           }
         }
       }
       ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+      if (!ok_run) break;
+      __syncwarp();
+      if (lane < kSub && my_phys >= 0) {
+        uint8_t *st = smem + kStageOff + s * kStageBytes;
+        const int u = j * kSub + lane;
+        const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          tma_load_2d(st + b * kAtomRows64 + lane * 2048, &kmap, b * 64, y, &kv_full[s], policy);
+          tma_load_2d(st + (2 + b) * kAtomRows64 + lane * 2048, &vmap, b * 64, y, &kv_full[s],
+                      policy);
+        }
+      }
     }
   }
 
@@ -554,28 +549,28 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 }
 
 // ---------------------------------------------------------------------------
-// Two query tiles per CTA, 64-key steps, scores double-buffered per tile.
+// Two query tiles per CTA, 64-key steps, scores and P in separate TMEM columns.
 //
 // One CTA per SM holds two 128-row tiles of the same (sequence, KV head) --
 // 256 rows = 256/G tokens x G heads -- and streams 64-key K/V steps through
 // two rings shared by both tiles (K and V apart, so a K stage is refilled as
 // soon as the Q K^T products that read it are done).  Each tile owns 256 TMEM
-// columns: two 64-column score buffers and O (128); P is written over the
-// scores it came from.  While a tile's softmax warps work on step n, the
-// tensor core already computes that tile's scores of step n + 1 and the other
-// tile's products, so both tiles' softmax warps can be busy at once and the
-// tensor core is fed from two independent streams.  Q is read from shared
-// memory (two 32 KB tiles).
+// columns: scores (64, fp32), P (64: two 32-column fp16 buffers, or one bf16
+// buffer of hi + lo parts) and O (128).  The softmax warps release the score
+// columns as soon as they have loaded them, so Q K^T of step n + 1 runs while
+// they work on step n, and P V of step n runs while they work on step n + 1.
+// Q is read from shared memory (two 32 KB tiles).
 // Warp roles: warps 0-3 softmax for tile 0, 4-7 for tile 1 (thread r of a
-// tile owns its row r and TMEM lane r), warps 8 and 9 issue the MMAs of tile
-// 0 and tile 1, warp 10 runs the TMA producer.  One thread issuing
-// tcgen05.mma back to back gets about one instruction per 120 cycles whatever
-// N is (measured on GB300), so each tile has its own issuing warp; the two
-// streams overlap on the tensor core.  V rows a product must not use (past the keys in use, or
-// in a sub-tile whose block id is out of range) are zeroed by the producer
-// before the stage is handed over; the softmax warps mask those keys.
+// tile owns its row r and TMEM lane r), warps 8-11 issue the MMAs (Q K^T of
+// tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1), warp 12 runs the TMA
+// producer.  One thread issuing tcgen05.mma back to back gets about one
+// instruction per 120 cycles whatever N is (measured on GB300), so the four
+// product streams have their own issuing warps and overlap on the tensor core.
+// V rows a product must not use (past the keys in use, or in a sub-tile whose
+// block id is out of range) are zeroed by the producer before the stage is
+// handed over; the softmax warps mask those keys.
 constexpr int kPairKeys = 64;                  // keys per step
-constexpr int kPairThreads = 352;              // 11 warps
+constexpr int kPairThreads = 416;              // 13 warps
 constexpr int kPairQAtom = kTcRows * 128;      // one 64-dim atom of a Q tile (bytes)
 constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V stage (bytes)
 
@@ -585,7 +580,7 @@ struct PairLayout {
   static constexpr int kKOff = 4 * kPairQAtom;                 // K ring: [SK][2 atoms]
   static constexpr int kVOff = kKOff + SK * 2 * kPairKvAtom;   // V ring: [SV][2 atoms]
   static constexpr int kBarOff = kVOff + SV * 2 * kPairKvAtom;
-  static constexpr int kBars = 2 * SK + 2 * SV + 1 + 4 + 2 + 2 + 1;
+  static constexpr int kBars = 2 * SK + 2 * SV + 1 + 2 + 2 + 4 + 4 + 1;
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
 };
 
@@ -597,6 +592,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+  // TMEM columns of a tile: scores 0..63, P 64..127, O 128..255.  fp16 P: two
+  // buffers of 32 columns (step n in buffer n % 2); bf16 P: one buffer, hi
+  // parts in 64..95 and lo parts in 96..127.
+  constexpr int kPBufs = SPLIT ? 1 : 2;
+  constexpr int kPCol = 64, kOCol = 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -606,10 +606,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint64_t *v_full = k_empty + SK;
   uint64_t *v_empty = v_full + SV;
   uint64_t *v_tail = v_empty + SV;     // the last step's V load, before its tail is zeroed
-  uint64_t *s_full = v_tail + 1;       // [2 tiles][2 buffers]
-  uint64_t *p_full = s_full + 4;       // [2 tiles]
-  uint64_t *pv_done = p_full + 2;      // [2 tiles]
-  uint64_t *q_ready = pv_done + 2;
+  uint64_t *s_full = v_tail + 1;       // [2 tiles]: scores computed
+  uint64_t *s_free = s_full + 2;       // [2 tiles]: scores loaded by the softmax warps
+  uint64_t *p_full = s_free + 2;       // [2 tiles][2 P buffers]
+  uint64_t *pv_done = p_full + 4;      // [2 tiles][2 P buffers]
+  uint64_t *q_ready = pv_done + 4;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
 
   const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
@@ -620,17 +621,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 2);  // released by both issuers
+      mbar_init(&k_empty[s], 2);  // released by both Q K^T issuers
     }
     for (int s = 0; s < SV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 2);
+      mbar_init(&v_empty[s], 2);  // and both P V issuers
     }
     mbar_init(v_tail, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&s_full[i], 1);
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&p_full[t], kTcRows);
-      mbar_init(&pv_done[t], 1);
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], kTcRows);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&p_full[i], kTcRows);
+      mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_ready, 2 * kTcRows);
     fence_barrier_init();
@@ -707,8 +711,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint32_t vmask_next = my_steps > 0 ? step_mask(0) : 0;
     for (int n = 0; n < my_steps && ok_run; ++n) {
       const uint32_t vmask = vmask_next;
-      const uint32_t sbuf = lane_addr + (n & 1) * kPairKeys;
-      if (!__all_sync(kFullMask, mbar_wait_bounded(&s_full[2 * t + (n & 1)], (n >> 1) & 1))) {
+      if (!__all_sync(kFullMask, mbar_wait_bounded(&s_full[t], n & 1))) {
         if (lane == 0) atomicOr(a.err, kErrTimeout);
         ok_run = false;
         break;
@@ -718,11 +721,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
       for (int q = 0; q < kPairKeys / 32; ++q) {
         float t0[32];
-        tmem_ld32(sbuf + 32 * q, t0);
+        tmem_ld32(lane_addr + 32 * q, t0);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
       }
+      // the score columns may now take the next step's Q K^T
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);
       if (n + 1 < my_steps) vmask_next = step_mask(n + 1);  // overlaps the softmax below
       const int key0 = n * kPairKeys;
       const bool full_step = row_ok && key0 + kPairKeys - 1 <= pos && vmask == kAllSub;
@@ -754,69 +760,74 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         m_ref = m_new;
       }
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      // P in 32-key chunks, each stored as soon as it is packed.  fp16: chunk c
-      // in columns 16c..16c+15 of the buffer (key k in column k/2).  bf16: hi
-      // and lo parts of chunk c in columns 32c..32c+15 and 32c+16..32c+31.
-      // Either way a chunk only overwrites scores this thread has already read.
-      // s scale - m and the row sum run on packed fp32 pairs.
+      // P for the whole step in registers first (s scale - m and the row sum on
+      // packed fp32 pairs), so the wait for its buffer below overlaps the math
       const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t negm2 = f2_pack(neg_m, neg_m);
       uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
+      uint32_t ph[kPairKeys / 2], pl[SPLIT ? kPairKeys / 2 : 1];
 #pragma unroll
-      for (int c = 0; c < kPairKeys / 32; ++c) {
-        uint32_t ph[16], pl[SPLIT ? 16 : 1];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]),
-                                            scale2, negm2));
-          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
-          ph[e] = Elem<T>::pack(p0, p1);
-          if constexpr (SPLIT) {
-            const float2 h = Elem<T>::unpack(ph[e]);
-            pl[e] = Elem<T>::pack(p0 - h.x, p1 - h.y);
-          }
-        }
+      for (int e = 0; e < kPairKeys / 2; ++e) {
+        const float2 x = f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), scale2, negm2));
+        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+        ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
+        ph[e] = Elem<T>::pack(p0, p1);
         if constexpr (SPLIT) {
-          tmem_st16(sbuf + 32 * c, ph);
-          tmem_st16(sbuf + 32 * c + 16, pl);
-        } else {
-          tmem_st16(sbuf + 16 * c, ph);
+          const float2 h = Elem<T>::unpack(ph[e]);
+          pl[e] = Elem<T>::pack(p0 - h.x, p1 - h.y);
         }
       }
       {
-        const float2 s = f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])));
-        l += s.x + s.y;
+        const float2 sm = f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])));
+        l += sm.x + sm.y;
       }
-      // P V of the previous step: waited for every step, so this warp is never
-      // more than one phase of pv_done behind (a parity wait cannot tell phase
-      // k from k + 2) and O holds every earlier product before it is rescaled
-      if (n > 0) {
-        if (!__all_sync(kFullMask, mbar_wait_bounded(&pv_done[t], (n - 1) & 1))) {
+      // O must hold P V of every earlier step before it is rescaled; P's buffer
+      // must have been read by the P V of step n - kPBufs.  Each pv_done
+      // barrier belongs to one buffer, and P V of step n cannot start before
+      // this warp arrives below, so no wait is more than one phase behind.
+      const int pb = n % kPBufs;
+      if (n > 0 && __any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
+        const int pp = (n - 1) % kPBufs;
+        if (!__all_sync(kFullMask, mbar_wait_bounded(&pv_done[2 * t + pp], ((n - 1) / kPBufs) & 1))) {
           if (lane == 0) atomicOr(a.err, kErrTimeout);
           ok_run = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
 #pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
-            float o[32];
-            tmem_ld32(lane_addr + 128 + cb * 32, o);
-            tmem_wait_ld();
+        for (int cb = 0; cb < 4; ++cb) {
+          float o[32];
+          tmem_ld32(lane_addr + kOCol + cb * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_addr + 128 + cb * 32, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_addr + kOCol + cb * 32, o);
+        }
+      }
+      if (n >= kPBufs &&
+          !__all_sync(kFullMask, mbar_wait_bounded(&pv_done[2 * t + pb], ((n - kPBufs) / kPBufs) & 1))) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        ok_run = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kPairKeys / 32; ++c) {
+        if constexpr (SPLIT) {
+          tmem_st16(lane_addr + kPCol + 16 * c, ph + 16 * c);
+          tmem_st16(lane_addr + kPCol + 32 + 16 * c, pl + 16 * c);
+        } else {
+          tmem_st16(lane_addr + kPCol + 32 * pb + 16 * c, ph + 16 * c);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&p_full[2 * t + pb]);
     }
     // ---- epilogue: O / l for this row
     if (ok_run && my_steps > 0) {
-      if (__all_sync(kFullMask, mbar_wait_bounded(&pv_done[t], (my_steps - 1) & 1))) {
+      const int last = my_steps - 1;
+      if (__all_sync(kFullMask, mbar_wait_bounded(&pv_done[2 * t + last % kPBufs], (last / kPBufs) & 1))) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T *orow = static_cast<T *>(a.out) +
@@ -824,7 +835,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float o[32];
-          tmem_ld32(lane_addr + 128 + cb * 32, o);
+          tmem_ld32(lane_addr + kOCol + cb * 32, o);
           tmem_wait_ld();
           if (row_ok) {
 #pragma unroll
@@ -842,89 +853,84 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         atomicOr(a.err, kErrTimeout);
       }
     }
-  } else if (active && (warp == 8 || warp == 9)) {
-    // ------------------------------------------------------- MMA issuer (tile)
-    // Per step n: Q K^T of step n + 1 (into the buffer P V of step n - 1
-    // read, so that product must be complete), then P V of step n once its P
-    // is in place.  The scores of step n + 1 are thus computed while the
-    // softmax warps work on step n.  Each issuer releases every K and V stage
-    // once (count-2 barriers); for steps its tile does not read it waits for
-    // the stage to fill first, so its release lands in that step's phase.
+  } else if (active && warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ MMA issuers
+    // Q K^T issuer of tile t: step n once the softmax warps have loaded the
+    // scores of step n - 1 and K of step n is in.  P V issuer: step n once its
+    // P and V are in place.  Each issuer releases every K (or V) stage once
+    // (count-2 barriers); for steps its tile does not read it waits for the
+    // stage to fill first, so its release lands in that step's phase.
     if (lane == 0) {
-      const int t = warp - 8;
+      const int t = (warp - 8) >> 1;
+      const bool qk_role = ((warp - 8) & 1) == 0;
       const int nt = t == 0 ? n_steps0 : n_steps1;
-      const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
-      const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
-      const uint32_t qb = smem_addr(smem + L::kQOff) + t * 2 * kPairQAtom;
-      const uint32_t sk0 = smem_addr(smem + L::kKOff), sv0 = smem_addr(smem + L::kVOff);
       const uint32_t tt = tmem + t * 256;
-      auto issue_qk = [&](int n) {
-        const uint32_t kb = sk0 + (n % SK) * 2 * kPairKvAtom;
-#pragma unroll
-        for (int k = 0; k < kTcDim / 16; ++k) {
-          const uint64_t da = umma_desc_sw128(qb + (k >> 2) * kPairQAtom + (k & 3) * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kPairKvAtom + (k & 3) * 32, 16, 1024);
-          umma_f16(tt + (n & 1) * kPairKeys, da, db, id_qk, k > 0);
-        }
-        umma_commit(&s_full[2 * t + (n & 1)]);
-        umma_commit(&k_empty[n % SK]);
-      };
-      bool ok_run = mbar_wait_bounded(q_ready, 0);
-      if (ok_run && nt > 0) {
-        ok_run = mbar_wait_bounded(&k_full[0], 0);
-        if (ok_run) {
-          tc_fence_after();
-          issue_qk(0);
-        }
-      }
-      for (int n = 0; n < nt && ok_run; ++n) {
-        if (n + 1 < nt) {
-          if ((n > 0 && !mbar_wait_bounded(&pv_done[t], (n - 1) & 1)) ||
-              !mbar_wait_bounded(&k_full[(n + 1) % SK], ((n + 1) / SK) & 1)) {
+      bool ok_run = true;
+      if (qk_role) {
+        const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
+        const uint32_t qb = smem_addr(smem + L::kQOff) + t * 2 * kPairQAtom;
+        const uint32_t sk0 = smem_addr(smem + L::kKOff);
+        ok_run = mbar_wait_bounded(q_ready, 0);
+        for (int n = 0; n < nt && ok_run; ++n) {
+          if ((n > 0 && !mbar_wait_bounded(&s_free[t], (n - 1) & 1)) ||
+              !mbar_wait_bounded(&k_full[n % SK], (n / SK) & 1)) {
             ok_run = false;
             break;
           }
           tc_fence_after();
-          issue_qk(n + 1);
-        }
-        const int s = n % SV;
-        if (!mbar_wait_bounded(&p_full[t], n & 1) || !mbar_wait_bounded(&v_full[s], (n / SV) & 1)) {
-          ok_run = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vb = sv0 + s * 2 * kPairKvAtom;
-        const uint32_t pcol = tt + (n & 1) * kPairKeys;
+          const uint32_t kb = sk0 + (n % SK) * 2 * kPairKvAtom;
 #pragma unroll
-        for (int kk = 0; kk < kPairKeys / 16; ++kk) {
-          const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kPairKvAtom, 1024);
-          if constexpr (SPLIT) {
-            const uint32_t hi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
-            umma_f16_ts(tt + 128, hi, dv, id_pv, n > 0 || kk > 0);
-            umma_f16_ts(tt + 128, hi + 16, dv, id_pv, true);
-          } else {
-            umma_f16_ts(tt + 128, pcol + 8 * kk, dv, id_pv, n > 0 || kk > 0);
+          for (int k = 0; k < kTcDim / 16; ++k) {
+            const uint64_t da = umma_desc_sw128(qb + (k >> 2) * kPairQAtom + (k & 3) * 32, 16, 1024);
+            const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kPairKvAtom + (k & 3) * 32, 16, 1024);
+            umma_f16(tt, da, db, id_qk, k > 0);
           }
+          umma_commit(&s_full[t]);
+          umma_commit(&k_empty[n % SK]);
         }
-        umma_commit(&pv_done[t]);
-        umma_commit(&v_empty[s]);
-      }
-      // stages of the steps this tile does not read
-      for (int m = nt; m < n_steps && ok_run; ++m) {
-        if (!mbar_wait_bounded(&k_full[m % SK], (m / SK) & 1)) {
-          ok_run = false;
-          break;
+        for (int m = nt; m < n_steps && ok_run; ++m) {
+          if (!mbar_wait_bounded(&k_full[m % SK], (m / SK) & 1)) {
+            ok_run = false;
+            break;
+          }
+          mbar_arrive(&k_empty[m % SK]);
         }
-        mbar_arrive(&k_empty[m % SK]);
-        if (!mbar_wait_bounded(&v_full[m % SV], (m / SV) & 1)) {
-          ok_run = false;
-          break;
+      } else {
+        const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
+        const uint32_t sv0 = smem_addr(smem + L::kVOff);
+        for (int n = 0; n < nt && ok_run; ++n) {
+          const int s = n % SV, pb = n % kPBufs;
+          if (!mbar_wait_bounded(&p_full[2 * t + pb], (n / kPBufs) & 1) ||
+              !mbar_wait_bounded(&v_full[s], (n / SV) & 1)) {
+            ok_run = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = sv0 + s * 2 * kPairKvAtom;
+#pragma unroll
+          for (int kk = 0; kk < kPairKeys / 16; ++kk) {
+            const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kPairKvAtom, 1024);
+            if constexpr (SPLIT) {
+              umma_f16_ts(tt + kOCol, tt + kPCol + 8 * kk, dv, id_pv, n > 0 || kk > 0);
+              umma_f16_ts(tt + kOCol, tt + kPCol + 32 + 8 * kk, dv, id_pv, true);
+            } else {
+              umma_f16_ts(tt + kOCol, tt + kPCol + 32 * pb + 8 * kk, dv, id_pv, n > 0 || kk > 0);
+            }
+          }
+          umma_commit(&pv_done[2 * t + pb]);
+          umma_commit(&v_empty[s]);
         }
-        mbar_arrive(&v_empty[m % SV]);
+        for (int m = nt; m < n_steps && ok_run; ++m) {
+          if (!mbar_wait_bounded(&v_full[m % SV], (m / SV) & 1)) {
+            ok_run = false;
+            break;
+          }
+          mbar_arrive(&v_empty[m % SV]);
+        }
       }
       if (!ok_run) atomicOr(a.err, kErrTimeout);
     }
-  } else if (active && warp == 10) {
+  } else if (active && warp == 12) {
     // ---------------------------------------------------------- TMA producer
     const int bs_mask = (1 << a.bs_log2) - 1;
     auto block_of = [&](int u) -> int {
@@ -945,26 +951,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         win_base += 32;
         win = block_of(win_base + lane);
       }
-      int phys[kSub];
-      uint32_t mask = 0;
-#pragma unroll
-      for (int h = 0; h < kSub; ++h) {
-        phys[h] = __shfl_sync(kFullMask, win, n * kSub + h - win_base);
-        if (phys[h] >= 0) mask |= 1u << h;
-      }
+      // lane h < kSub issues the copies of sub-tile h: one thread issuing TMA
+      // copies back to back gets through one every ~150 cycles, so the step's
+      // 16 copies are spread over four lanes
+      const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
+      const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
       const uint32_t bytes = __popc(mask) * 2 * 2048;
       auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
-#pragma unroll
-        for (int h = 0; h < kSub; ++h) {
-          if (phys[h] < 0) continue;
-          const int u = n * kSub + h;
-          const int y = ((phys[h] * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
+        if (lane < kSub && my_phys >= 0) {
+          const int u = n * kSub + lane;
+          const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
 #pragma unroll
           for (int b = 0; b < 2; ++b)
-            tma_load_2d(st + b * kPairKvAtom + h * 2048, map, b * 64, y, bar, policy);
+            tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
         }
       };
-      // K
+      // K: the expected bytes are posted (lane 0) before any lane issues a copy
       const int sk = n % SK;
       if (lane == 0) {
         if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
@@ -973,11 +975,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           mbar_arrive(&k_full[sk]);
         } else {
           mbar_arrive_expect_tx(&k_full[sk], bytes);
-          load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
         }
       }
       ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
       if (!ok_run) break;
+      __syncwarp();
+      load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
       // V: rows past the keys in use and sub-tiles not loaded become zeros
       const int sv = n % SV;
       uint8_t *vst = smem + L::kVOff + sv * 2 * kPairKvAtom;
@@ -985,6 +988,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         ok_run = false;
       ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
       if (!ok_run) break;
+      __syncwarp();
       const int key0 = n * kPairKeys;
       const bool tail = key0 + kPairKeys > n_keys;
       if (mask != kAllSub) {
@@ -1000,26 +1004,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       __syncwarp();
       if (!tail) {
         if (lane == 0) {
-          if (bytes == 0) {
+          if (bytes == 0)
             mbar_arrive(&v_full[sv]);
-          } else {
+          else
             mbar_arrive_expect_tx(&v_full[sv], bytes);
-            load(vst, &vmap, &v_full[sv]);
-          }
         }
+        __syncwarp();
+        load(vst, &vmap, &v_full[sv]);
       } else {
         // the last step: load, wait, zero the rows past n_keys, then hand over
+        if (lane == 0 && bytes > 0) mbar_arrive_expect_tx(v_tail, bytes);
+        __syncwarp();
+        load(vst, &vmap, v_tail);
         bool got = true;
-        if (lane == 0 && bytes > 0) {
-          mbar_arrive_expect_tx(v_tail, bytes);
-          load(vst, &vmap, v_tail);
-          got = mbar_wait_bounded(v_tail, 0);
-        }
+        if (lane == 0 && bytes > 0) got = mbar_wait_bounded(v_tail, 0);
         got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
         if (!got) {
           ok_run = false;
           break;
         }
+        __syncwarp();
         const int first = n_keys - key0;  // first row to clear
         for (int i = lane; i < kPairKeys * 2 * 8; i += 32) {
           const int row = i >> 4, b = (i >> 3) & 1, u16 = i & 7;
@@ -1036,7 +1040,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
 
   // ---- teardown: every tcgen05 operation is complete once each tile's last
-  // pv_done phase has been observed by its softmax warps (or it had no work)
+  // P V has been observed by its softmax warps (its Q K^T products came
+  // before it), or the tile had no work
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
