@@ -562,15 +562,16 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 // Q is read from shared memory (two 32 KB tiles).
 // Warp roles: warps 0-3 softmax for tile 0, 4-7 for tile 1 (thread r of a
 // tile owns its row r and TMEM lane r), warps 8-11 issue the MMAs (Q K^T of
-// tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1), warp 12 runs the TMA
-// producer.  One thread issuing tcgen05.mma back to back gets about one
-// instruction per 120 cycles whatever N is (measured on GB300), so the four
-// product streams have their own issuing warps and overlap on the tensor core.
+// tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1), warps 12 and 13 load
+// K and V.  One thread issuing tcgen05.mma back to back gets about one
+// instruction per 120 cycles whatever N is, and a warp issuing a step's TMA
+// copies takes about as long as the step's softmax (measured on GB300), so
+// every stream has its own warp.
 // V rows a product must not use (past the keys in use, or in a sub-tile whose
 // block id is out of range) are zeroed by the producer before the stage is
 // handed over; the softmax warps mask those keys.
 constexpr int kPairKeys = 64;                  // keys per step
-constexpr int kPairThreads = 416;              // 13 warps
+constexpr int kPairThreads = 448;              // 14 warps
 constexpr int kPairQAtom = kTcRows * 128;      // one 64-dim atom of a Q tile (bytes)
 constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V stage (bytes)
 
@@ -930,8 +931,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       if (!ok_run) atomicOr(a.err, kErrTimeout);
     }
-  } else if (active && warp == 12) {
-    // ---------------------------------------------------------- TMA producer
+  } else if (active && warp >= 12) {
+    // --------------------------------------------- TMA producers (12: K, 13: V)
+    const bool k_role = warp == 12;
     const int bs_mask = (1 << a.bs_log2) - 1;
     auto block_of = [&](int u) -> int {
       if (u >= n_sub) return -1;
@@ -951,9 +953,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         win_base += 32;
         win = block_of(win_base + lane);
       }
-      // lane h < kSub issues the copies of sub-tile h: one thread issuing TMA
-      // copies back to back gets through one every ~150 cycles, so the step's
-      // 16 copies are spread over four lanes
+      // lane h < kSub issues the copies of sub-tile h
       const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
       const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
       const uint32_t bytes = __popc(mask) * 2 * 2048;
@@ -966,21 +966,24 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
         }
       };
-      // K: the expected bytes are posted (lane 0) before any lane issues a copy
-      const int sk = n % SK;
-      if (lane == 0) {
-        if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
-          ok_run = false;
-        } else if (bytes == 0) {
-          mbar_arrive(&k_full[sk]);
-        } else {
-          mbar_arrive_expect_tx(&k_full[sk], bytes);
+      if (k_role) {
+        // the expected bytes are posted (lane 0) before any lane issues a copy
+        const int sk = n % SK;
+        if (lane == 0) {
+          if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
+            ok_run = false;
+          } else if (bytes == 0) {
+            mbar_arrive(&k_full[sk]);
+          } else {
+            mbar_arrive_expect_tx(&k_full[sk], bytes);
+          }
         }
+        ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+        if (!ok_run) break;
+        __syncwarp();
+        load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
+        continue;
       }
-      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
-      if (!ok_run) break;
-      __syncwarp();
-      load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
       // V: rows past the keys in use and sub-tiles not loaded become zeros
       const int sv = n % SV;
       uint8_t *vst = smem + L::kVOff + sv * 2 * kPairKvAtom;
