@@ -730,7 +730,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // the score columns may now take the next step's Q K^T
       tc_fence_before();
       mbar_arrive(&s_free[t]);
-      if (n + 1 < my_steps) vmask_next = step_mask(n + 1);  // overlaps the softmax below
+      // block id of sub-tile `lane` of step n + 1: loaded now, used at the end
+      // of the step, so its latency hides behind the softmax
+      int bt_next = -1;
+      {
+        const int u = (n + 1) * kSub + lane;
+        if (n + 1 < my_steps && lane < kSub && u < n_sub) bt_next = bt_row[(u * 16) >> a.bs_log2];
+      }
       const int key0 = n * kPairKeys;
       const bool full_step = row_ok && key0 + kPairKeys - 1 <= pos && vmask == kAllSub;
       if (!full_step) {
@@ -824,6 +830,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[2 * t + pb]);
+      vmask_next =
+          __ballot_sync(kFullMask, bt_next >= 0 && static_cast<int64_t>(bt_next) < a.num_blocks) &
+          kAllSub;
     }
     // ---- epilogue: O / l for this row
     if (ok_run && my_steps > 0) {
