@@ -60,6 +60,10 @@ CASES = [
     ("llama3_70b_cb", dict(lens=[130, 1000, 31], chunk=65)),                      # G = 8, bs 32
     ("llama3_70b_cb", dict(lens=[300, 64], chunk=10**6, head_dim=64, dtype="bf16")),
     ("llama3_8b_gqa", dict(lens=[100, 40], chunk=10**6, num_q_heads=8, num_kv_heads=8)),  # G = 1
+    ("llama3_8b_gqa", dict(lens=[900, 300, 77], chunk=200, num_q_heads=16, num_kv_heads=8)),  # G = 2
+    ("llama3_8b_gqa", dict(lens=[500, 64], chunk=50, num_q_heads=16, num_kv_heads=8,
+                           dtype="bf16")),                                  # G = 2, one-tile kernel
+    ("llama3_70b_cb", dict(lens=[700, 1200], chunk=150, dtype="bf16")),     # G = 8, bf16, bs 32
 ]
 
 
