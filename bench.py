@@ -396,24 +396,32 @@ def run_ours(args):
     if pa.pa_device_errors(stream) != 0:
         raise RuntimeError("device error bits raised during the decode / graph timing")
 
-    # end to end through the public API with host buffers: per step, pinned
-    # host -> device copies of the step's inputs, the step, and the output back
-    host = {n: t.pin_memory() for n, t in (("q", w.query), ("key", w.key), ("value", w.value),
-                                           ("sm", w.slot_mapping), ("bt", w.block_tables),
-                                           ("cl", w.context_lens))}
-    dq, dkey, dval = torch.empty_like(q), torch.empty_like(key), torch.empty_like(value)
-    dsm, dbt, dcl = torch.empty_like(sm), torch.empty_like(bt), torch.empty_like(cl)
+    # end to end through the public API with host buffers: per step, the
+    # step's inputs go host -> device in one copy from a pinned staging buffer
+    # (each input in its own 256-byte-aligned segment, as a serving loop would
+    # stage them), then the step, then the output back to pinned host memory
+    segs = (("q", w.query), ("key", w.key), ("value", w.value), ("sm", w.slot_mapping),
+            ("bt", w.block_tables), ("cl", w.context_lens))
+    offs, total = {}, 0
+    for n, t in segs:
+        offs[n] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    hstage = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dstage = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def seg_view(buf, n, t):
+        nbytes = t.numel() * t.element_size()
+        return buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+
+    for n, t in segs:
+        seg_view(hstage, n, t).copy_(t)
+    dq, dkey, dval, dsm, dbt, dcl = (seg_view(dstage, n, t) for n, t in segs)
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = total
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
-        dq.copy_(host["q"], non_blocking=True)
-        dkey.copy_(host["key"], non_blocking=True)
-        dval.copy_(host["value"], non_blocking=True)
-        dsm.copy_(host["sm"], non_blocking=True)
-        dbt.copy_(host["bt"], non_blocking=True)
-        dcl.copy_(host["cl"], non_blocking=True)
+        dstage.copy_(hstage, non_blocking=True)
         scatter(dkey, dval, dsm, stream)
         decode(dq, dbt, dcl, stream)
         hout.copy_(out, non_blocking=True)
