@@ -128,12 +128,14 @@ def test_prefill_bench_size_repeatable(pa, dtype):
         assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
 
 
-@pytest.mark.parametrize("chunk", [300, 20])   # two-tile kernel, one-tile kernel (G = 4)
-def test_prefill_bad_block_flagged_others_exact(pa, chunk):
+@pytest.mark.parametrize("chunk,head_dim", [(300, 128), (20, 128), (40, 64)],
+                         ids=["two-tile", "one-tile", "mma-sync"])
+def test_prefill_bad_block_flagged_others_exact(pa, chunk, head_dim):
     """An out-of-range block id in one sequence's table: the call flags it,
     reads nothing through it (that sequence's rows stay finite), and every
     other sequence's rows still match the oracle."""
-    pw = W.make_prefill("llama3_8b_gqa", 65, lens=[700, 1400, 900], chunk=chunk)
+    pw = W.make_prefill("llama3_8b_gqa", 65, lens=[700, 1400, 900], chunk=chunk,
+                        head_dim=head_dim)
     dev = torch.device("cuda")
     kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
     pa.pa_reshape_and_cache(pw.key.to(dev), pw.value.to(dev), kc, vc, pw.slot_mapping.to(dev))
