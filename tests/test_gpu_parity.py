@@ -141,6 +141,29 @@ def test_small_cases_all_partition_sizes(pa, name, kw):
     check_decode(run)
 
 
+def _random_decode(i):
+    """Seeded random decode shape: batch 1-8, contexts 0-3000, group 1-8,
+    1-8 KV heads, head_dim 64 or 128, block size 16 or 32, fp16 or bf16."""
+    rng = np.random.default_rng(2000 + i)
+    G = int(rng.integers(1, 9))
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    lens = [int(x) for x in rng.integers(0, 3001, int(rng.integers(1, 9)))]
+    return dict(lens=lens, num_q_heads=G * hkv, num_kv_heads=hkv,
+                head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([16, 32])),
+                dtype=str(rng.choice(["fp16", "bf16"])))
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_decode_random_shapes(pa, i):
+    w = W.make("llama3_8b_gqa", 90 + i, **_random_decode(i))
+    ps = int(np.random.default_rng(3000 + i).choice([0, 16, 48, 160, 512]))
+    run = Run(pa, w, partition_sizes=[ps])
+    assert run.err == 0
+    kh, vh = run.host_pool()
+    assert np.array_equal(u16(run.kc), kh) and np.array_equal(u16(run.vc), vh)
+    check_decode(run)
+
+
 def test_empty_batch(pa):
     dev = torch.device("cuda")
     kc = torch.zeros(4, 2, 16, 64, dtype=torch.float16, device=dev)

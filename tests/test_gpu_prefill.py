@@ -158,3 +158,25 @@ def test_prefill_bad_block_flagged_others_exact(pa, chunk, head_dim):
         got = out[a:b].float().cpu().double().numpy()
         err = np.abs(got - ref)
         assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
+
+
+def _random_case(i):
+    """Seeded random prefill shape: batch 1-4, contexts up to 1500, chunk 1-600,
+    group 1/2/4/8 at head_dim 128 (both tcgen05 kernels), block size 16 or 32,
+    fp16 or bf16."""
+    rng = np.random.default_rng(1000 + i)
+    G = int(rng.choice([1, 2, 4, 8]))
+    hkv = int(rng.choice([1, 2, 4]))
+    batch = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.integers(1, 1501, batch)]
+    chunk = int(rng.choice([1, 7, 33, 64, 100, 257, 600]))
+    return dict(lens=lens, chunk=chunk, num_q_heads=G * hkv, num_kv_heads=hkv,
+                block_size=int(rng.choice([16, 32])), dtype=str(rng.choice(["fp16", "bf16"])))
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_prefill_random_shapes(pa, i):
+    pw = W.make_prefill("llama3_8b_gqa", 70 + i, **_random_case(i))
+    kc, vc, out, err = run(pa, pw)
+    assert err == 0
+    check(pw, kc, vc, out)
