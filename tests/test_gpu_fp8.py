@@ -92,6 +92,22 @@ def test_fp8_full_size(pa, name):
     check(w, kh, vh, outs, pairs=[(i, h) for i in seqs for h in range(w.num_q_heads)])
 
 
+@pytest.mark.parametrize("i", range(12))
+def test_fp8_random_shapes(pa, i):
+    """Seeded random FP8 decode shapes: batch 1-8, contexts 0-3000, group 1-8,
+    1-8 KV heads, block size 16 or 32, one partition size each."""
+    rng = np.random.default_rng(4000 + i)
+    G, hkv = int(rng.integers(1, 9)), int(rng.choice([1, 2, 4, 8]))
+    lens = [int(x) for x in rng.integers(0, 3001, int(rng.integers(1, 9)))]
+    w = W.to_fp8(W.make("llama3_8b_gqa", 120 + i, lens=lens, num_q_heads=G * hkv,
+                        num_kv_heads=hkv, block_size=int(rng.choice([16, 32]))))
+    ps = int(rng.choice([0, 16, 48, 160, 512]))
+    kc, vc, outs = run_fp8(pa, w, [ps])
+    kh, vh = host_pool(w)
+    assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
+    check(w, kh, vh, outs)
+
+
 def test_fp8_scatter_from_bf16_and_saturation(pa):
     """bf16 source rows, and values far past the E4M3 range, quantise exactly
     as the oracle does (saturating at +-448)."""
