@@ -331,6 +331,16 @@ pa_status pa_decode_static_workspace(void *out, const void *query,
  */
 pa_status pa_device_errors(void *stream, uint32_t *flags);
 
+/*
+ * Self-test of the device-side wait limit (no counterpart on the pages; it
+ * exists so the failure path of every staged-data wait can be exercised
+ * without a fault).  Launches one CTA on `stream` that waits on a barrier
+ * nothing ever completes; the wait gives up after its limit (about 1 s),
+ * sets PA_DEVERR_TIMEOUT in the device error word and the CTA exits, leaving
+ * the context usable.  Returns after the launch: PA_OK or PA_ERR_CUDA.
+ */
+pa_status pa_selftest_bounded_wait(void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(int32_t status);
 

@@ -24,7 +24,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_reduce", "pa_decode_workspace_size",
     "pa_decode_num_partitions", "pa_device_errors", "pa_status_string", "library_path",
     "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
-    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill", "pa_selftest_bounded_wait",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
 ]
 
@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
             L.pa_decode_reduce.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P]
             L.pa_decode_reduce.restype = i32
             L.pa_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.pa_selftest_bounded_wait.argtypes = [P]
+            L.pa_selftest_bounded_wait.restype = i32
             L.pa_device_errors.restype = i32
             L.pa_status_string.argtypes = [i32]
             L.pa_status_string.restype = ctypes.c_char_p
@@ -374,6 +376,12 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor
                            block_tables.shape[1], context_lens.data_ptr(), B, int(max_q_len), Hq,
                            Hkv, d, bs, NB, float(scale), _dtype_code(k_cache), _stream(stream)))
     return out
+
+
+def pa_selftest_bounded_wait(stream=None) -> None:
+    """Launch the wait-limit self-test: one CTA waits on a barrier nothing
+    completes, gives up after about a second and sets DEVERR_TIMEOUT."""
+    _check("pa_selftest_bounded_wait", _load().pa_selftest_bounded_wait(_stream(stream)))
 
 
 def pa_device_errors(stream=None) -> int:

@@ -439,6 +439,14 @@ pa_status pa_swap_blocks(const void *src, void *dst, const int64_t *block_mappin
              : PA_ERR_CUDA;
 }
 
+pa_status pa_selftest_bounded_wait(void *stream) {
+  unsigned int *err = nullptr;
+  if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
+  return pa::launch_selftest_wait(err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_device_errors(void *stream, uint32_t *flags) {
   if (!flags) return PA_ERR_INVALID_ARG;
   unsigned int *err = nullptr;

@@ -66,4 +66,26 @@ cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStrea
                           dim3(kThreads), 0, stream, a);
 }
 
+namespace {
+
+// Waits on a barrier whose phase never completes: every thread's bounded wait
+// gives up after kWaitLimitNs and the CTA reports it and exits.
+__global__ void selftest_wait_kernel(unsigned *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait_bounded(&bar, 0);
+  if (!done && threadIdx.x == 0) atomicOr(err, kErrTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError();
+}
+
 }  // namespace pa

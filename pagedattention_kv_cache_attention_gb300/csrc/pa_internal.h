@@ -102,4 +102,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void
                            int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
                            bool *map_failed);
 
+// One CTA waiting on a barrier nothing completes (the wait-limit self-test).
+cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t stream);
+
 }  // namespace pa

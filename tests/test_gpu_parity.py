@@ -300,3 +300,21 @@ def test_bad_slot_and_length_flags(pa):
     assert pa.pa_device_errors() & pa.DEVERR_BAD_LEN
     assert torch.all(out[1] == 0)
     assert pa.pa_device_errors() == 0   # the word was cleared
+
+
+def test_bounded_wait_gives_up_and_context_survives(pa):
+    """The wait limit every staged-data wait uses: a CTA waiting on a barrier
+    nothing completes gives up after about a second and reports
+    PA_DEVERR_TIMEOUT, without a fault; the context then still runs a decode
+    that matches the oracle."""
+    import time
+    assert pa.pa_device_errors() == 0
+    t0 = time.perf_counter()
+    pa.pa_selftest_bounded_wait()
+    flags = pa.pa_device_errors()          # waits for the stream
+    dt = time.perf_counter() - t0
+    assert flags & pa.DEVERR_TIMEOUT
+    assert 0.5 < dt < 30, dt
+    run = Run(pa, W.make("tiny_mha", 7))
+    assert run.err == 0
+    check_decode(run)
