@@ -585,3 +585,14 @@ PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_pin(pin):
     pin()
+
+
+def test_generator_slots_are_distinct():
+    """Every generated batch honours the scatter's contract (no two new tokens
+    in one slot), and the check rejects a duplicate."""
+    for name in W.NAMES:
+        W.check_distinct_slots(W.make(name, 3).slot_mapping)
+    W.check_distinct_slots(W.make_prefill("llama3_8b_gqa", 3, batch=4, chunk=100).slot_mapping)
+    W.check_distinct_slots([5, -1, -1, 7])
+    with pytest.raises(ValueError):
+        W.check_distinct_slots([5, 9, 5])

@@ -215,6 +215,7 @@ def _build(name, seed, dtype, B, Hq, Hkv, d, bs, ctx: np.ndarray, pool_slack: fl
     key = _randn((B, Hkv, d), gen, dtype)
     value = _randn((B, Hkv, d), gen, dtype)
     scale = float(np.float32(1.0 / math.sqrt(d)))
+    check_distinct_slots(slots)
     return Workload(name=name, dtype=dtype, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,
                     head_dim=d, block_size=bs, num_blocks=NB, scale=scale,
                     partition_size=partition_size,
@@ -222,6 +223,15 @@ def _build(name, seed, dtype, B, Hq, Hkv, d, bs, ctx: np.ndarray, pool_slack: fl
                     block_tables=torch.from_numpy(bt), slot_mapping=torch.from_numpy(slots),
                     query=query, key=key, value=value, k_cache=k_cache, v_cache=v_cache,
                     seed=seed)
+
+
+def check_distinct_slots(slots) -> None:
+    """The scatter's contract: no two new tokens of one call share a slot
+    (slot < 0 = no token).  Raises ValueError on a duplicate."""
+    s = np.asarray(slots, dtype=np.int64)
+    s = s[s >= 0]
+    if np.unique(s).size != s.size:
+        raise ValueError("duplicate slot in slot_mapping")
 
 
 NAMES = ("tiny_mha", "llama3_8b_gqa", "shared_prefix_cow", "long_context", "llama3_70b_cb")
@@ -353,6 +363,7 @@ def make_prefill(name: str, seed: int = 0, *, chunk: int = 512,
             v = cache[blk, :, off, :]
             _poison(v, w.dtype)
             cache[blk, :, off, :] = v
+    check_distinct_slots(slots)
     gen = torch.Generator().manual_seed(seed + 7919)
     return PrefillWorkload(
         **{f.name: getattr(w, f.name) for f in dataclasses.fields(Workload)
