@@ -364,6 +364,43 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
+    # spread of the step time: 10 blocks of 5 back-to-back steps (events only
+    # at block ends), and single steps after an L2 flush (a 2x-L2 memset, then
+    # the step between events) -- neither enters `value`
+    def pct(xs, f):
+        xs = sorted(xs)
+        return xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+
+    blocks = []
+    for _ in range(10):
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(5):
+            step()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        blocks.append(b0.elapsed_time(b1) / 5)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flushed = []
+    for _ in range(20):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        f0.record(stream)
+        step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        flushed.append(f0.elapsed_time(f1))
+    del flush
+    step_stats = {
+        "blocks_of_5_ms": {"median": round(statistics.median(blocks), 5),
+                           "p10": round(pct(blocks, 0.1), 5), "p90": round(pct(blocks, 0.9), 5)},
+        "l2_flushed_ms": {"median": round(statistics.median(flushed), 5),
+                          "p10": round(pct(flushed, 0.1), 5), "p90": round(pct(flushed, 0.9), 5)},
+    }
+    if pa.pa_device_errors(stream) != 0:
+        raise RuntimeError("device error bits raised during the spread measurement")
+
     # the same step replayed from a CUDA graph (no host work per step)
     graph_ms = None
     try:
@@ -479,6 +516,7 @@ def run_ours(args):
                 "ms_per_step": round(graph_ms, 5),
                 "value": round(world * ab["step"] / (graph_ms * 1e-3) / 1e9, 2), "unit": "GB/s"},
             "hbm_fraction": round(value_gbs / world / peak, 4),
+            "step_stats": step_stats,
             "bytes_per_step": ab,
             "roofline": {"bound": "hbm", "kernel": "pa_decode (main kernel + LSE reduce), "
                                                     "K event-bracketed calls after the timed steps",
