@@ -37,6 +37,9 @@ if ROOT not in sys.path:
 METRIC = "paged-decode KV GB/s (fraction of GB300 HBM peak); decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+# layers of the model each batch is shaped after (Llama-3-8B: 32, Llama-3-70B: 80)
+MODEL_LAYERS = {"llama3_8b_gqa": 32, "shared_prefix_cow": 32, "long_context": 32,
+                "llama3_70b_cb": 80}
 DEFAULT_WORKLOAD = "llama3_8b_gqa"
 DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
 
@@ -512,6 +515,12 @@ def run_ours(args):
                        "l2": f"no flush: inputs larger than L2 ({ab['kv'] / 1e6:.0f} MB of KV "
                              f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2)"},
             "decode_tokens_per_s": round(world * w.num_seqs / (ms_per_step * 1e-3), 1),
+            # one attention layer per step; the full model has n_layers of them
+            # (attention only: no projections or MLPs counted)
+            "attention_only_full_model_tokens_per_s": {
+                "layers": MODEL_LAYERS.get(w.name),
+                "value": (round(world * w.num_seqs / (ms_per_step * 1e-3) / MODEL_LAYERS[w.name], 1)
+                          if w.name in MODEL_LAYERS else None)},
             "graph_replay": None if graph_ms is None else {
                 "ms_per_step": round(graph_ms, 5),
                 "value": round(world * ab["step"] / (graph_ms * 1e-3) / 1e9, 2), "unit": "GB/s"},
