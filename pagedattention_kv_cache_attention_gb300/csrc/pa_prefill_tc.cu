@@ -1,42 +1,14 @@
 // pa_prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
-// core (tcgen05: accumulators and two of the operands in tensor memory).
+// core (tcgen05: accumulators and P in tensor memory, operands staged by TMA).
 //
 // Same computation as pa_prefill.cu ("Serving engines", How vLLM works:
 // chunked prefill; chunk row t at position ctx - q_len + t attends causally to
 // tokens 0..t's position through the block table), for head_dim 128 and query
-// groups G in {1, 2, 4, 8}.
-//
-// One CTA per (128 query rows, KV head, sequence); the rows are 128/G tokens x
-// G heads of one KV group.  Q and P are the A operands of the two products and
-// live in tensor memory next to the accumulators, so shared memory only holds
-// the K/V ring and the tensor core reads just K and V from it (a 32-key step
-// reads 16 KB of shared memory instead of 56 KB with Q and P there).
-// Warp roles:
-//  * warps 0-3 (128 threads): thread r owns query row r and TMEM lane r.  They
-//    write Q into tensor memory once, then per KEYS-key step read the scores
-//    row, apply the causal mask, run the online softmax and write P
-//    (fp16/bf16 pairs) over the scores it came from: one FFMA and one
-//    ex2.approx per score, masks only on steps that cross a row's position,
-//    tree reductions for the row max and sum.  The running max is only moved
-//    -- and O in TMEM rescaled -- when a row's max grows by more than 2^8;
-//    between moves P may exceed 1 (at most 256), which fp16/bf16 carry exactly
-//    as far as their precision goes, and numerator and denominator share the
-//    same reference.  In the last step they zero V rows past the keys in use,
-//    so tail slots (whatever they hold) cannot reach O.
-//  * warp 4, one thread: issues S = Q K^T (M 128, N KEYS, K 128: 8 MMAs, Q
-//    from TMEM) into one of two TMEM score buffers and O += P V (M 128, N 128,
-//    K KEYS, P from TMEM, V an MN-major shared-memory operand), committing each
-//    to an mbarrier.  S for step j+1 is in flight while the softmax warps work
-//    on step j; S for step j+2 reuses step j's buffer once P V of step j (which
-//    reads P there) has completed.
-//  * warp 5, one thread: stages KEYS-key K/V steps (16-row sub-tiles, two
-//    128-byte boxes each for K and V) through the block table with 2-D TMA into
-//    a ring of S stages, refilling a stage once the P V product that read it
-//    has completed.
-// TMEM (KEYS = 32: 256 columns, so two CTAs share an SM): scores/P in columns
-// 0..2 KEYS, Q in the next 64 (two 16-bit values per column), O in 128-255.
-// bf16 carries P as hi + lo parts (two P V MMAs), so P keeps ~16 bits; the lo
-// part sits in the second half of the score buffer.
+// groups G in {1, 2, 4, 8}.  One kernel template, two shapes: two 128-row
+// query tiles per CTA (one CTA per SM) for chunks longer than 128/G tokens,
+// one tile per CTA (two CTAs per SM) for shorter ones.  The design and the
+// measurements that shaped it are described above the kernel.
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -76,10 +48,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
       : "memory");
 }
 
-// Where each operand lives.  32-key steps keep Q in TMEM (64 columns next to
-// two 32-column score buffers and O); 64-key steps need 128 columns of score
-// buffers, so Q is read from shared memory (128-byte swizzled, K-major).  Both
-// fit 256 columns, so two CTAs share an SM.
 // Packed fp32 pairs (sm_100 and later): two IEEE fp32 operations per instruction,
 // each rounded exactly as the scalar one.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
@@ -108,462 +76,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-template <int KEYS>
-struct TcLayout {
-  static constexpr bool kQInTmem = KEYS == 32;
-  static constexpr int kSCol = 0;                          // score buffers: [2][KEYS]
-  static constexpr int kQCol = 2 * KEYS;                   // Q in TMEM: 64 columns
-  static constexpr int kOCol = 128;                        // O: 128 columns
-  static constexpr int kCols = 256;
-  static constexpr int kAtomRows64 = KEYS * 128;           // one 64-dim atom of a step (bytes)
-  static constexpr int kAtomRows128 = kTcRows * 128;       // one 64-dim atom of Q (bytes)
-  static constexpr int kQBytes = kQInTmem ? 0 : 2 * kAtomRows128;
-  static constexpr int kStageBytes = 4 * kAtomRows64;      // K: 2 atoms, V: 2 atoms
-  static_assert(KEYS == 32 || KEYS == 64, "32- or 64-key steps");
-  static_assert(!kQInTmem || kQCol + 64 <= kOCol, "Q overlaps O");
-  static_assert(2 * KEYS <= kOCol, "scores overlap O");
-};
-
-template <typename T, int S, bool SPLIT, int KEYS>
-__global__ void __launch_bounds__(192, 2)
-    pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
-  using L = TcLayout<KEYS>;
-  constexpr int kTcKeys = KEYS;                 // keys per step
-  constexpr int kAtomRows64 = L::kAtomRows64;
-  constexpr int kSub = kTcKeys / 16;            // 16-row sub-tiles per step
-  constexpr uint32_t kAllSub = (1u << kSub) - 1;
-  constexpr int kStageBytes = L::kStageBytes;
-  constexpr int kStageOff = L::kQBytes;
-  constexpr int kBarOff = kStageOff + S * kStageBytes;
-  constexpr int kPCols = kTcKeys / 2;           // P of one step: two 16-bit values per column
-  constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
-  static_assert(!SPLIT || 2 * kPCols <= kTcKeys, "P hi + lo must fit the score buffer");
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-  uint64_t *kv_empty = kv_full + S;
-  uint64_t *s_full = kv_empty + S;  // [2]
-  uint64_t *p_full = s_full + 2;
-  uint64_t *pv_done = p_full + 1;
-  uint64_t *q_ready = pv_done + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
-  uint32_t *step_valid = tmem_slot + 1;  // [S]: bit h = sub-tile h of the step was loaded
-
-  const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = a.group;
-  const int tpc = kTcRows / G;
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kTcRows);
-    mbar_init(pv_done, 1);
-    mbar_init(q_ready, kTcRows);
-    fence_barrier_init();
-  }
-  if (warp == 4) tmem_alloc(tmem_slot, L::kCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  grid_dependency_wait();  // the chunk's K/V may come from the kernel before
-
-  const int q0 = a.query_start[seq];
-  const int q_len = a.query_start[seq + 1] - q0;
-  const int ctx = a.context_lens[seq];
-  bool active = true;
-  if (q_len < 0 || ctx < q_len || ctx > (a.max_blocks_per_seq << a.bs_log2) ||
-      q_len > a.max_q_len) {
-    if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
-    active = false;
-  }
-  const int t_first = tile * tpc;
-  if (t_first >= q_len) active = false;
-  const int t_last = min(q_len, t_first + tpc) - 1;
-  const int base_pos = ctx - q_len;
-  const int n_keys = base_pos + t_last + 1;
-  const int n_steps = active ? (n_keys + kTcKeys - 1) / kTcKeys : 0;
-
-  if (active && warp < 4) {
-    // ------------------------------------------------------------ softmax warps
-    const int r = tid;
-    const int tok = t_first + r / G;
-    const bool row_ok = r < tpc * G && tok <= t_last;
-    const int pos = base_pos + tok;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    {
-      const T *qrow = static_cast<const T *>(a.query) +
-                      (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
-                       r % G) * kTcDim;
-      if constexpr (L::kQInTmem) {
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          uint32_t qv[16];
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + part * 32 + ch * 8)
-                                   : make_uint4(0, 0, 0, 0);
-            qv[4 * ch] = v.x;
-            qv[4 * ch + 1] = v.y;
-            qv[4 * ch + 2] = v.z;
-            qv[4 * ch + 3] = v.w;
-          }
-          tmem_st16(lane_addr + L::kQCol + part * 16, qv);
-        }
-        tmem_wait_st();
-      } else {
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
-                                 : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * L::kAtomRows128 + r * 128 +
-                                     (((ch & 7) ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(q_ready);
-
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok_run = true;
-    for (int j = 0; j < n_steps && ok_run; ++j) {
-      const int s = j % S;
-      const uint32_t sbuf = lane_addr + L::kSCol + (j & 1) * kTcKeys;
-      // warp-uniform decisions: the TMEM loads and stores below are warp-collective
-      const bool got = mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1) &&
-                       mbar_wait_bounded(&kv_full[s], (j / S) & 1);
-      if (!__all_sync(kFullMask, got)) {
-        if (lane == 0) atomicOr(a.err, kErrTimeout);
-        ok_run = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[kTcKeys];
-#pragma unroll
-      for (int q = 0; q < kTcKeys / 32; ++q) {
-        float t0[32];
-        tmem_ld32(sbuf + 32 * q, t0);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
-      }
-      const int key0 = j * kTcKeys;
-      const uint32_t vmask = step_valid[s];
-      // zero V rows this step must not use: past the keys in use, or never loaded
-      bool zeroed = false;
-      if (key0 + kTcKeys > n_keys || vmask != kAllSub) {
-        const int kr = r >> 1, atom = r & 1;
-        if (kr < kTcKeys && (key0 + kr >= n_keys || !((vmask >> (kr >> 4)) & 1u))) {
-          uint4 *row = reinterpret_cast<uint4 *>(smem + kStageOff + s * kStageBytes +
-                                                 (2 + atom) * kAtomRows64 + kr * 128);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
-        }
-        zeroed = true;
-      }
-      // mask (only steps that reach past the row's position or hold an
-      // unloaded sub-tile need it) and the row max of the raw scores
-      const bool full_step = row_ok && key0 + kTcKeys - 1 <= pos && vmask == kAllSub;
-      if (!full_step) {
-#pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          const int key = key0 + c;
-          const bool ok = row_ok && key <= pos && ((vmask >> (c >> 4)) & 1u);
-          sv[c] = ok ? sv[c] : -INFINITY;
-        }
-      }
-      constexpr int kCh = kTcKeys / 8;  // 8-score chunks
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kCh; ++i) {
-        mx[i & 7] = fmaxf(mx[i & 7],
-                          fmaxf(fmaxf(fmaxf(sv[8 * i], sv[8 * i + 1]), fmaxf(sv[8 * i + 2], sv[8 * i + 3])),
-                                fmaxf(fmaxf(sv[8 * i + 4], sv[8 * i + 5]), fmaxf(sv[8 * i + 6], sv[8 * i + 7]))));
-      }
-      const float tmax_raw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float tmax = tmax_raw * a.scale_log2;  // the scale is positive: same order
-      const float m_new = fmaxf(m_ref, tmax);
-      const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
-      const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - m_new));
-      if (move) {
-        l *= alpha;
-        m_ref = m_new;
-      }
-      // P = 2^(s scale - m): one FFMA and one ex2 per score; a row with no key
-      // yet (m = -inf) gets 2^-inf = 0 everywhere
-      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t ph[kPCols], pl[SPLIT ? kPCols : 1];
-      float ls[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < kCh; ++ch) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pv[e] = ex2_approx(fmaf(sv[ch * 8 + e], a.scale_log2, neg_m));
-        ls[ch & 7] += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          ph[ch * 4 + e] = Elem<T>::pack(pv[2 * e], pv[2 * e + 1]);
-          if constexpr (SPLIT) {
-            const float2 f = Elem<T>::unpack(ph[ch * 4 + e]);
-            pl[ch * 4 + e] = Elem<T>::pack(pv[2 * e] - f.x, pv[2 * e + 1] - f.y);
-          }
-        }
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // P over the scores it came from: the buffer is this step's alone (step
-      // j-2's P V completed before S of step j was issued into it)
-#pragma unroll
-      for (int c = 0; c < kPCols; c += 16) {
-        tmem_st16(sbuf + c, ph + c);
-        if constexpr (SPLIT) tmem_st16(sbuf + kPCols + c, pl + c);
-      }
-      // P V of the previous step: waited for every step, so this warp is never
-      // more than one phase of pv_done behind (a parity wait cannot tell phase
-      // k from k + 2) and O holds every earlier product before it is rescaled
-      if (j > 0) {
-        if (!__all_sync(kFullMask, mbar_wait_bounded(pv_done, (j - 1) & 1))) {
-          if (lane == 0) atomicOr(a.err, kErrTimeout);
-          ok_run = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(kFullMask, move)) {  // whole warp: rows that did not move use 1
-#pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
-            float o[32];
-            tmem_ld32(lane_addr + L::kOCol + cb * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_addr + L::kOCol + cb * 32, o);
-          }
-        }
-      }
-      tmem_wait_st();
-      if (zeroed) fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // ---- epilogue: O / l for this row
-    if (ok_run && n_steps > 0) {
-      if (__all_sync(kFullMask, mbar_wait_bounded(pv_done, (n_steps - 1) & 1))) {
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        T *orow = static_cast<T *>(a.out) +
-                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + r % G) * kTcDim;
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float o[32];
-          tmem_ld32(lane_addr + L::kOCol + cb * 32, o);
-          tmem_wait_ld();
-          if (row_ok) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 pk;
-              pk.x = Elem<T>::pack(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
-              pk.y = Elem<T>::pack(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
-              pk.z = Elem<T>::pack(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
-              pk.w = Elem<T>::pack(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
-              *reinterpret_cast<uint4 *>(orow + cb * 32 + q * 8) = pk;
-            }
-          }
-        }
-      } else if (lane == 0) {
-        atomicOr(a.err, kErrTimeout);
-      }
-    }
-  } else if (active && warp == 4) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kTcKeys);
-      const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
-      const uint32_t sst = smem_addr(smem + kStageOff), sq = smem_addr(smem);
-      bool ok_run = mbar_wait_bounded(q_ready, 0);
-      if (ok_run) tc_fence_after();
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % S;
-        if (!mbar_wait_bounded(&kv_full[s], (j / S) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kb = sst + s * kStageBytes;
-#pragma unroll
-        for (int k = 0; k < kTcDim / 16; ++k) {
-          const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kAtomRows64 + (k & 3) * 32, 16, 1024);
-          if constexpr (L::kQInTmem) {
-            umma_f16_ts(tmem + L::kSCol + (j & 1) * kTcKeys, tmem + L::kQCol + k * 8, db, id_qk,
-                        k > 0);
-          } else {
-            const uint64_t da =
-                umma_desc_sw128(sq + (k >> 2) * L::kAtomRows128 + (k & 3) * 32, 16, 1024);
-            umma_f16(tmem + L::kSCol + (j & 1) * kTcKeys, da, db, id_qk, k > 0);
-          }
-        }
-        umma_commit(&s_full[j & 1]);
-        return true;
-      };
-      if (ok_run) ok_run = issue_qk(0);
-      if (ok_run && n_steps > 1) ok_run = issue_qk(1);
-      for (int j = 0; j < n_steps && ok_run; ++j) {
-        if (!mbar_wait_bounded(p_full, j & 1)) {
-          ok_run = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vb = sst + (j % S) * kStageBytes + 2 * kAtomRows64;
-        const uint32_t pa_col = tmem + L::kSCol + (j & 1) * kTcKeys;
-#pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
-          umma_f16_ts(tmem + L::kOCol, pa_col + kk * 8, dv, id_pv, j > 0 || kk > 0);
-        }
-        if constexpr (SPLIT) {
-#pragma unroll
-          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kAtomRows64, 1024);
-            umma_f16_ts(tmem + L::kOCol, pa_col + kPCols + kk * 8, dv, id_pv, true);
-          }
-        }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[j % S]);
-        // S of step j+2 goes where P of step j is: wait for this P V to finish
-        if (j + 2 < n_steps) {
-          if (!mbar_wait_bounded(pv_done, j & 1)) {
-            ok_run = false;
-            break;
-          }
-          tc_fence_after();
-          if (!issue_qk(j + 2)) {
-            ok_run = false;
-            break;
-          }
-        }
-      }
-      if (!ok_run) atomicOr(a.err, kErrTimeout);
-    }
-  } else if (active && warp == 5) {
-    // ---------------------------------------------------------- TMA producer
-    const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
-    const int n_sub = (n_keys + 15) / 16;
-    const int bs_mask = (1 << a.bs_log2) - 1;
-    auto block_of = [&](int u) -> int {
-      if (u >= n_sub) return -1;
-      const int phys = bt_row[(u * 16) >> a.bs_log2];
-      if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
-        atomicOr(a.err, kErrBadBlock);
-        return -1;
-      }
-      return phys;
-    };
-    const uint64_t policy = l2_policy_evict_first();
-    int win_base = 0;
-    int win = block_of(lane);
-    bool ok_run = true;
-    for (int j = 0; j < n_steps && ok_run; ++j) {
-      const int s = j % S;
-      if (j * kSub >= win_base + 32) {
-        win_base += 32;
-        win = block_of(win_base + lane);
-      }
-      // lane h < kSub issues the four copies of sub-tile h (one thread gets
-      // through a TMA copy every ~150 cycles)
-      const int my_phys = __shfl_sync(kFullMask, win, j * kSub + (lane & (kSub - 1)) - win_base);
-      const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
-      const uint32_t bytes = __popc(mask) * 4 * 2048;
-      if (lane == 0) {
-        if (j >= S && !mbar_wait_bounded(&kv_empty[s], ((j / S) - 1) & 1)) {
-          atomicOr(a.err, kErrTimeout);
-          ok_run = false;
-        } else {
-          step_valid[s] = mask;
-          if (bytes == 0) {
-            mbar_arrive(&kv_full[s]);
-          } else {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&kv_full[s], bytes);
-          }
-        }
-      }
-      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
-      if (!ok_run) break;
-      __syncwarp();
-      if (lane < kSub && my_phys >= 0) {
-        uint8_t *st = smem + kStageOff + s * kStageBytes;
-        const int u = j * kSub + lane;
-        const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          tma_load_2d(st + b * kAtomRows64 + lane * 2048, &kmap, b * 64, y, &kv_full[s], policy);
-          tma_load_2d(st + (2 + b) * kAtomRows64 + lane * 2048, &vmap, b * 64, y, &kv_full[s],
-                      policy);
-        }
-      }
-    }
-  }
-
-  // ---- teardown: every tcgen05 operation is complete once pv_done's last
-  // phase has been observed by the softmax warps (or the CTA had no work)
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 4) {
-    tc_fence_after();
-    tmem_dealloc(tmem, L::kCols);
-  }
-  grid_launch_dependents();
-}
-
-template <typename T, int S, bool SPLIT, int KEYS>
-cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
-                                cudaStream_t stream) {
-  constexpr size_t smem = 1024 + TcLayout<KEYS>::kQBytes +
-                          static_cast<size_t>(S) * TcLayout<KEYS>::kStageBytes +
-                          (2 * S + 5) * 8 + 8 + S * 4;
-  auto kern = pa_prefill_tc_kernel<T, S, SPLIT, KEYS>;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  const int tpc = kTcRows / a.group;
-  const int tiles = (a.max_q_len + tpc - 1) / tpc;
-  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(192), smem, stream,
-                          km, vm, a);
-}
-
 // ---------------------------------------------------------------------------
-// Two query tiles per CTA, 64-key steps, scores and P in separate TMEM columns.
+// Query tiles per CTA, 64-key steps, scores and P in separate TMEM columns.
 //
-// One CTA per SM holds two 128-row tiles of the same (sequence, KV head) --
-// 256 rows = 256/G tokens x G heads -- and streams 64-key K/V steps through
-// two rings shared by both tiles (K and V apart, so a K stage is refilled as
-// soon as the Q K^T products that read it are done).  Each tile owns 256 TMEM
+// A CTA holds TILES (1 or 2) 128-row tiles of the same (sequence, KV head) --
+// 128 TILES rows = 128 TILES / G tokens x G heads -- and streams 64-key K/V
+// steps through two rings shared by its tiles (K and V apart, so a K stage is
+// refilled as soon as the Q K^T products that read it are done).  Two tiles
+// take all 512 TMEM columns and one CTA per SM; one tile takes 256 and two
+// CTAs share an SM.  Each tile owns 256 TMEM
 // columns: scores (64, fp32), P (64: two 32-column fp16 buffers, or one bf16
 // buffer of hi + lo parts) and O (128).  The softmax warps release the score
 // columns as soon as they have loaded them, so Q K^T of step n + 1 runs while
 // they work on step n, and P V of step n runs while they work on step n + 1.
 // Q is read from shared memory (two 32 KB tiles).
-// Warp roles: warps 0-3 softmax for tile 0, 4-7 for tile 1 (thread r of a
-// tile owns its row r and TMEM lane r), warps 8-11 issue the MMAs (Q K^T of
-// tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1), warps 12 and 13 load
-// K and V.  One thread issuing tcgen05.mma back to back gets about one
+// Warp roles (two tiles): warps 0-3 softmax for tile 0, 4-7 for tile 1
+// (thread r of a tile owns its row r and TMEM lane r), warps 8-11 issue the
+// MMAs (Q K^T of tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1),
+// warps 12 and 13 load K and V; with one tile the same roles in warps 0-7.  One thread issuing tcgen05.mma back to back gets about one
 // instruction per 120 cycles whatever N is, and a warp issuing a step's TMA
 // copies takes about as long as the step's softmax (measured on GB300), so
 // every stream has its own warp.
@@ -571,25 +101,32 @@ cudaError_t launch_prefill_tc_t(const PrefillArgs &a, const CUtensorMap &km, con
 // block id is out of range) are zeroed by the producer before the stage is
 // handed over; the softmax warps mask those keys.
 constexpr int kPairKeys = 64;                  // keys per step
-constexpr int kPairThreads = 448;              // 14 warps
 constexpr int kPairQAtom = kTcRows * 128;      // one 64-dim atom of a Q tile (bytes)
 constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V stage (bytes)
 
-template <int SK, int SV>
+// TILES query tiles per CTA: softmax warps 0 .. 4 TILES - 1, issuing warps
+// 4 TILES .. 6 TILES - 1 (Q K^T and P V of each tile), then the K and V warps.
+template <int TILES>
+constexpr int pair_threads() { return 32 * (6 * TILES + 2); }
+
+template <int SK, int SV, int TILES>
 struct PairLayout {
-  static constexpr int kQOff = 0;                              // Q: [2 tiles][2 atoms]
-  static constexpr int kKOff = 4 * kPairQAtom;                 // K ring: [SK][2 atoms]
+  static constexpr int kQOff = 0;                              // Q: [TILES][2 atoms]
+  static constexpr int kKOff = TILES * 2 * kPairQAtom;         // K ring: [SK][2 atoms]
   static constexpr int kVOff = kKOff + SK * 2 * kPairKvAtom;   // V ring: [SV][2 atoms]
   static constexpr int kBarOff = kVOff + SV * 2 * kPairKvAtom;
   static constexpr int kBars = 2 * SK + 2 * SV + 1 + 2 + 2 + 4 + 4 + 1;
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
 };
 
-template <typename T, int SK, int SV, bool SPLIT>
-__global__ void __launch_bounds__(kPairThreads, 1)
+template <typename T, int SK, int SV, bool SPLIT, int TILES>
+__global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
-  using L = PairLayout<SK, SV>;
+  static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
+  using L = PairLayout<SK, SV, TILES>;
+  constexpr int kIssue0 = 4 * TILES;      // first MMA-issuing warp
+  constexpr int kLoad0 = 6 * TILES;       // K producer warp (V: kLoad0 + 1)
   constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
@@ -617,16 +154,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.group;
-  const int tpc = 2 * kTcRows / G;     // tokens per CTA
+  const int tpc = TILES * kTcRows / G; // tokens per CTA
 
   if (tid == 0) {
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 2);  // released by both Q K^T issuers
+      mbar_init(&k_empty[s], TILES);  // released by every Q K^T issuer
     }
     for (int s = 0; s < SV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 2);  // and both P V issuers
+      mbar_init(&v_empty[s], TILES);  // and every P V issuer
     }
     mbar_init(v_tail, 1);
     for (int t = 0; t < 2; ++t) {
@@ -637,10 +174,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(&p_full[i], kTcRows);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(q_ready, 2 * kTcRows);
+    mbar_init(q_ready, TILES * kTcRows);
     fence_barrier_init();
   }
-  if (warp == 8) tmem_alloc(tmem_slot, 512);
+  if (warp == kIssue0) tmem_alloc(tmem_slot, 256 * TILES);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -664,7 +201,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // holds the later tokens, so it reads every step tile 0 reads
   const int half = kTcRows / G;
   const int last0 = min(t_last, t_first + half - 1);
-  const int last1 = t_first + half <= t_last ? t_last : -1;
+  const int last1 = TILES == 2 && t_first + half <= t_last ? t_last : -1;
   const int n_keys = base_pos + t_last + 1;
   const int n_steps0 = active ? (base_pos + last0 + 1 + kPairKeys - 1) / kPairKeys : 0;
   const int n_steps1 = active && last1 >= 0 ? (n_keys + kPairKeys - 1) / kPairKeys : 0;
@@ -672,7 +209,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
   const int n_sub = (n_keys + 15) / 16;
 
-  if (active && warp < 8) {
+  if (active && warp < kIssue0) {
     // ------------------------------------------------------------ softmax warps
     const int t = warp >> 2;
     const int r = tid & (kTcRows - 1);                 // row within the tile = TMEM lane
@@ -863,7 +400,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         atomicOr(a.err, kErrTimeout);
       }
     }
-  } else if (active && warp >= 8 && warp < 12) {
+  } else if (active && warp >= kIssue0 && warp < kLoad0) {
     // ------------------------------------------------------------ MMA issuers
     // Q K^T issuer of tile t: step n once the softmax warps have loaded the
     // scores of step n - 1 and K of step n is in.  P V issuer: step n once its
@@ -871,8 +408,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // (count-2 barriers); for steps its tile does not read it waits for the
     // stage to fill first, so its release lands in that step's phase.
     if (lane == 0) {
-      const int t = (warp - 8) >> 1;
-      const bool qk_role = ((warp - 8) & 1) == 0;
+      const int t = (warp - kIssue0) >> 1;
+      const bool qk_role = ((warp - kIssue0) & 1) == 0;
       const int nt = t == 0 ? n_steps0 : n_steps1;
       const uint32_t tt = tmem + t * 256;
       bool ok_run = true;
@@ -940,9 +477,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       if (!ok_run) atomicOr(a.err, kErrTimeout);
     }
-  } else if (active && warp >= 12) {
-    // --------------------------------------------- TMA producers (12: K, 13: V)
-    const bool k_role = warp == 12;
+  } else if (active && warp >= kLoad0) {
+    // ---------------------------------------------------- TMA producers (K, V)
+    const bool k_role = warp == kLoad0;
     const int bs_mask = (1 << a.bs_log2) - 1;
     auto block_of = [&](int u) -> int {
       if (u >= n_sub) return -1;
@@ -1056,19 +593,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // before it), or the tile had no work
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kIssue0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 256 * TILES);
   }
   grid_launch_dependents();
 }
 
-template <typename T, int SK, int SV, bool SPLIT>
+template <typename T, int SK, int SV, bool SPLIT, int TILES>
 cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km,
                                      const CUtensorMap &vm, cudaStream_t stream) {
-  constexpr size_t smem = PairLayout<SK, SV>::kSmem;
-  static_assert(smem <= 227 * 1024, "shared memory");
-  auto kern = pa_prefill_tc_pair_kernel<T, SK, SV, SPLIT>;
+  constexpr size_t smem = PairLayout<SK, SV, TILES>::kSmem;
+  static_assert(smem <= (TILES == 1 ? 113 : 227) * 1024, "shared memory");
+  auto kern = pa_prefill_tc_pair_kernel<T, SK, SV, SPLIT, TILES>;
   static bool configured[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1080,23 +617,20 @@ cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int tpc = 2 * kTcRows / a.group;
+  const int tpc = TILES * kTcRows / a.group;
   const int tiles = (a.max_q_len + tpc - 1) / tpc;
-  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(kPairThreads), smem,
+  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(pair_threads<TILES>()), smem,
                           stream, km, vm, a);
 }
 
 }  // namespace
 
-// 32-key steps take 256 TMEM columns, so two CTAs (two softmax warps per
-// scheduler, two MMA streams) share an SM; each holds a ring of 16 KB K/V stages.
-#ifndef PA_PREFILL_TC_STAGES
-#define PA_PREFILL_TC_STAGES 6
+#ifndef PA_PREFILL_SOLO_KSTAGES
+#define PA_PREFILL_SOLO_KSTAGES 2
 #endif
-#ifndef PA_PREFILL_TC_KEYS
-#define PA_PREFILL_TC_KEYS 32
+#ifndef PA_PREFILL_SOLO_VSTAGES
+#define PA_PREFILL_SOLO_VSTAGES 2
 #endif
-
 #ifndef PA_PREFILL_PAIR_KSTAGES
 #define PA_PREFILL_PAIR_KSTAGES 4
 #endif
@@ -1108,24 +642,24 @@ bool prefill_tc_supported(int head_dim, int group) {
   return head_dim == kTcDim && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
-// Chunks that fill more than one 128-row tile go to the two-tile kernel; the
-// rest (short chunks, decode-like rows) to the 32-key kernel, which runs two
-// CTAs per SM.
+// Chunks that fill more than one 128-row tile run with two tiles per CTA (one
+// CTA per SM); shorter ones (short chunks, decode-like rows) with one tile per
+// CTA, two CTAs per SM.
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                               int dtype, cudaStream_t stream) {
   const bool pair = static_cast<int64_t>(a.max_q_len) * a.group > kTcRows;
   if (dtype == 0) {
     if (pair)
       return launch_prefill_tc_pair_t<__half, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
-                                      false>(a, km, vm, stream);
-    return launch_prefill_tc_t<__half, PA_PREFILL_TC_STAGES, false, PA_PREFILL_TC_KEYS>(a, km, vm,
-                                                                                      stream);
+                                      false, 2>(a, km, vm, stream);
+    return launch_prefill_tc_pair_t<__half, PA_PREFILL_SOLO_KSTAGES, PA_PREFILL_SOLO_VSTAGES, false,
+                                    1>(a, km, vm, stream);
   }
   if (pair)
     return launch_prefill_tc_pair_t<__nv_bfloat16, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
-                                    true>(a, km, vm, stream);
-  return launch_prefill_tc_t<__nv_bfloat16, PA_PREFILL_TC_STAGES, true, PA_PREFILL_TC_KEYS>(a, km, vm,
-                                                                                           stream);
+                                    true, 2>(a, km, vm, stream);
+  return launch_prefill_tc_pair_t<__nv_bfloat16, PA_PREFILL_SOLO_KSTAGES, PA_PREFILL_SOLO_VSTAGES,
+                                  true, 1>(a, km, vm, stream);
 }
 
 }  // namespace pa
