@@ -82,24 +82,25 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // A CTA holds TILES (1 or 2) 128-row tiles of the same (sequence, KV head) --
 // 128 TILES rows = 128 TILES / G tokens x G heads -- and streams 64-key K/V
 // steps through two rings shared by its tiles (K and V apart, so a K stage is
-// refilled as soon as the Q K^T products that read it are done).  Two tiles
-// take all 512 TMEM columns and one CTA per SM; one tile takes 256 and two
-// CTAs share an SM.  Each tile owns 256 TMEM
-// columns: scores (64, fp32), P (64: two 32-column fp16 buffers, or one bf16
-// buffer of hi + lo parts) and O (128).  The softmax warps release the score
-// columns as soon as they have loaded them, so Q K^T of step n + 1 runs while
-// they work on step n, and P V of step n runs while they work on step n + 1.
-// Q is read from shared memory (two 32 KB tiles).
+// refilled as soon as the Q K^T products that read it are done).  Each tile
+// owns 256 TMEM columns: scores (64, fp32), P (64: two 32-column fp16 buffers,
+// or one bf16 buffer of hi + lo parts) and O (128).  Two tiles take all 512
+// columns and one CTA per SM; one tile takes 256 and two CTAs share an SM.
+// The softmax warps release the score columns as soon as they have loaded
+// them, so Q K^T of step n + 1 runs while they work on step n, and P V of step
+// n runs while they work on step n + 1.  Q is read from shared memory (one
+// 32 KB tile per query tile).
+//
 // Warp roles (two tiles): warps 0-3 softmax for tile 0, 4-7 for tile 1
 // (thread r of a tile owns its row r and TMEM lane r), warps 8-11 issue the
 // MMAs (Q K^T of tile 0, P V of tile 0, Q K^T of tile 1, P V of tile 1),
-// warps 12 and 13 load K and V; with one tile the same roles in warps 0-7.  One thread issuing tcgen05.mma back to back gets about one
-// instruction per 120 cycles whatever N is, and a warp issuing a step's TMA
-// copies takes about as long as the step's softmax (measured on GB300), so
-// every stream has its own warp.
-// V rows a product must not use (past the keys in use, or in a sub-tile whose
-// block id is out of range) are zeroed by the producer before the stage is
-// handed over; the softmax warps mask those keys.
+// warps 12 and 13 load K and V; one tile has the same roles in warps 0-7.
+// One thread issuing tcgen05.mma back to back gets about one instruction per
+// 120 cycles whatever N is, and a warp issuing a step's TMA copies takes about
+// as long as the step's softmax (measured on GB300), so every stream has its
+// own warp.  V rows a product must not use (past the keys in use, or in a
+// sub-tile whose block id is out of range) are zeroed by the V loader before
+// the stage is handed over; the softmax warps mask those keys.
 constexpr int kPairKeys = 64;                  // keys per step
 constexpr int kPairQAtom = kTcRows * 128;      // one 64-dim atom of a Q tile (bytes)
 constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V stage (bytes)
