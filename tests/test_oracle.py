@@ -579,6 +579,38 @@ def pin_prefill_chunks_compose():
         assert np.array_equal(two, one[rows])
 
 
+def pin_random_shapes_vs_brute_force():
+    """Seeded sweep of small random shapes (group 1-8, 1/2/4 KV heads, head_dim
+    64/128, block size 16/32, fp16/bf16, contexts 0-300): the oracle's decode
+    equals the textbook non-paged attention (numpy gather + softmax) to 1e-12,
+    and its prefill of each sequence's last rows equals the decode of the
+    sequence cut at each row's position (bit for bit)."""
+    for i in range(16):
+        rng = np.random.default_rng(5000 + i)
+        G, hkv = int(rng.integers(1, 9)), int(rng.choice([1, 2, 4]))
+        lens = [int(x) for x in rng.integers(0, 301, int(rng.integers(1, 5)))]
+        kw = dict(lens=lens, num_q_heads=G * hkv, num_kv_heads=hkv,
+                  head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([16, 32])),
+                  dtype=str(rng.choice(["fp16", "bf16"])))
+        w = W.make("llama3_8b_gqa", 200 + i, **kw)
+        kc, vc = _after_scatter(w)
+        got = oracle.decode(w.query, kc, vc, w.block_tables, w.context_lens, w.scale, w.dtype)
+        assert np.allclose(got, _brute(w, kc, vc), rtol=1e-12, atol=1e-13), i
+        pw = W.make_prefill("llama3_8b_gqa", 300 + i, chunk=int(rng.integers(1, 40)),
+                            **dict(kw, lens=[max(1, x) for x in lens]))
+        pkc, pvc = _prefill_pool(pw)
+        rows = oracle.prefill(pw.query, pw.query_start, pkc, pvc, pw.block_tables,
+                              pw.context_lens, pw.scale, pw.dtype)
+        for s in range(pw.num_seqs):
+            ql = int(pw.query_start[s + 1] - pw.query_start[s])
+            for t in range(ql):
+                row = int(pw.query_start[s]) + t
+                pos = int(pw.context_lens[s]) - ql + t
+                ref = oracle.decode(pw.query[row:row + 1], pkc, pvc, pw.block_tables[s:s + 1],
+                                    np.array([pos + 1], np.int32), pw.scale, pw.dtype)
+                assert np.array_equal(rows[row], ref[0]), (i, s, t)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
