@@ -531,6 +531,26 @@ __global__ void __launch_bounds__(kReduceRows * 32) pa_decode_reduce_kernel(cons
   const float *l = a.ws_l + row * a.num_parts;
   const float *o = a.ws_o + row * a.num_parts * D + lane * kPer;
 
+  // the partials of up to kPre partitions are loaded together with (m, l), so
+  // the common case (a handful of partitions) takes one round trip after the
+  // context length instead of two
+  constexpr int kPre = 8;
+  float xo[kPre][kPer];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    if (u < np) {
+      if constexpr (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(o + static_cast<int64_t>(u) * D);
+        xo[u][0] = v.x;
+        xo[u][1] = v.y;
+        xo[u][2] = v.z;
+        xo[u][3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) xo[u][e] = o[static_cast<int64_t>(u) * D + e];
+      }
+    }
+  }
   float M = -INFINITY;
   for (int p = lane; p < np; p += 32) M = fmaxf(M, m[p]);
 #pragma unroll
@@ -550,6 +570,17 @@ __global__ void __launch_bounds__(kReduceRows * 32) pa_decode_reduce_kernel(cons
     L += wgt;
     const int cnt = min(32, np - p0);
     int j = 0;
+    if (p0 == 0) {
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        if (u < cnt) {
+          const float wj = __shfl_sync(kFull, wgt, u);
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) acc[e] += wj * xo[u][e];
+        }
+      }
+      j = min(cnt, kPre);
+    }
     for (; j + 4 <= cnt; j += 4) {
       float x[4][kPer];
 #pragma unroll
