@@ -97,6 +97,9 @@ def _check(call: str, status: int) -> None:
 def _cuda(name: str, t: torch.Tensor, dtype=None) -> None:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.get_device() != torch.cuda.current_device():
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, but the calls run on the current "
+                         f"device cuda:{torch.cuda.current_device()}")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
@@ -184,6 +187,8 @@ def pa_decode_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: t
     _cuda("out", out)
     _cuda("workspace", workspace)
     _cuda("context_lens", context_lens, torch.int32)
+    if not (out.is_contiguous() and workspace.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("out, workspace and context_lens must be contiguous")
     B, Hq, d = out.shape
     _check("pa_decode_reduce", _load().pa_decode_reduce(
         out.data_ptr(), workspace.data_ptr(), context_lens.data_ptr(), B, Hq, d,

@@ -318,3 +318,27 @@ def test_bounded_wait_gives_up_and_context_survives(pa):
     run = Run(pa, W.make("tiny_mha", 7))
     assert run.err == 0
     check_decode(run)
+
+
+def test_binding_rejects_bad_tensors_before_launch(pa):
+    """The Python binding refuses strided views, wrong dtypes and wrong shapes
+    with ValueError before anything is launched."""
+    w = W.make("tiny_mha", 8)
+    dev = torch.device("cuda")
+    q, kc, vc = w.query.to(dev), w.k_cache.to(dev), w.v_cache.to(dev)
+    bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    bad = [
+        dict(query=q.transpose(0, 1).contiguous().transpose(0, 1)),   # strided view
+        dict(block_tables=bt.to(torch.int64)),                        # wrong dtype
+        dict(out=torch.empty(q.shape[0], q.shape[1] + 1, q.shape[2], dtype=q.dtype, device=dev)),
+        dict(query=w.query),                                          # host tensor
+    ]
+    for kw in bad:
+        args = dict(out=out, query=q, k_cache=kc, v_cache=vc, block_tables=bt, context_lens=cl)
+        args.update(kw)
+        with pytest.raises(ValueError):
+            pa.pa_decode(args["out"], args["query"], args["k_cache"], args["v_cache"],
+                         args["block_tables"], args["context_lens"], w.scale, w.max_context_len, 0)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() == 0
