@@ -4,18 +4,21 @@ A step is the whole hot path over one batch: pa_reshape_and_cache (write each
 sequence's newest K/V through its slot) then pa_decode (paged attention, with
 split-context partitions joined by log-sum-exp when the workload uses them).
 
-Default workload: the Llama-3-8B-shaped GQA decode batch (64 sequences, 32
-query / 8 KV heads, head_dim 128, block_size 16, context lengths U[512,4096],
-fp16, 512-token partitions).  Inputs are seeded synthetic data resident in HBM;
-the KV bytes read per step (~0.6 GB) exceed the 129 MB L2, so no flush is
-needed between steps.
+Default workload: the Llama-3-70B-shaped continuous-batching decode batch (256
+sequences, 64 query / 8 KV heads, head_dim 128, block_size 32, context lengths
+lognormal with median 1024 clipped to [1, 16384], fp16, 1024-token partitions),
+the largest of the decode batches.  Measured in the same run and reported
+under `extra_workloads`: the Llama-3-8B-shaped GQA batch (64 sequences, 32/8
+heads, block_size 16, context lengths U[512,4096], fp16) and the 70B batch in
+bf16.  Inputs are seeded synthetic data resident in HBM; the KV bytes read per
+step (0.6-1.8 GB) exceed the 129 MB L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  `value` is KV GB/s: algorithmic bytes per step
 (K and V of exactly the context tokens, q in and out, the block-table entries
 and context lengths read, the scattered rows) over the device time per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--dtype fp16|bf16] [--impl ours|reference]
+                    [--dtype fp16|bf16] [--impl ours|reference] [--extra NAME:DTYPE]
 """
 from __future__ import annotations
 
@@ -40,7 +43,9 @@ L2_BYTES = 129 * 1024 * 1024
 # layers of the model each batch is shaped after (Llama-3-8B: 32, Llama-3-70B: 80)
 MODEL_LAYERS = {"llama3_8b_gqa": 32, "shared_prefix_cow": 32, "long_context": 32,
                 "llama3_70b_cb": 80}
-DEFAULT_WORKLOAD = "llama3_8b_gqa"
+DEFAULT_WORKLOAD = "llama3_70b_cb"
+# the other decode targets measured beside the default line, in the same run
+DEFAULT_EXTRAS = ("llama3_8b_gqa:fp16", "llama3_70b_cb:bf16")
 DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
 
 
@@ -192,12 +197,32 @@ def make_workload(args):
     return w
 
 
-def cpu_oracle_run(w, budget_s: float):
+def cpu_model() -> str:
+    """Name of the host CPU (lscpu's model name, else /proc/cpuinfo, else the
+    machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
+def cpu_oracle_run(w, budget_s: float, threads: int = 0):
     """Time the oracle (scatter + fp64 decode) on a bounded sample: the first
     n sequences, n grown until one run takes a good part of the budget; when
     the whole batch is quicker than that, the run is repeated until about two
-    thirds of the budget is spent.  Returns (GB/s, cores, sample description,
-    seconds, n)."""
+    thirds of the budget is spent.  ``threads`` = 0 uses every host core.
+    Returns (GB/s, threads used, sample description, seconds, n)."""
     import numpy as np
     import torch
 
@@ -208,7 +233,7 @@ def cpu_oracle_run(w, budget_s: float):
     else:
         kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
         vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
-    cores = oracle.max_threads()
+    cores = threads if threads > 0 else oracle.max_threads()
 
     def one_run(n):
         sub = slice(0, n)
@@ -219,7 +244,7 @@ def cpu_oracle_run(w, budget_s: float):
         else:
             oracle.reshape_and_cache(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub])
         oracle.decode(w.query[sub], kh, vh, w.block_tables[sub], w.context_lens[sub], w.scale,
-                      w.dtype, partition_size=w.partition_size,
+                      w.dtype, partition_size=w.partition_size, threads=threads,
                       kv_dtype="e4m3" if fp8 else None, k_scale=w.k_scale, v_scale=w.v_scale)
         return time.perf_counter() - t0
 
@@ -240,8 +265,19 @@ def cpu_oracle_run(w, budget_s: float):
             + 4 * ((ctx + w.block_size - 1) // w.block_size).sum() + 4 * n
             + 2 * n * w.num_kv_heads * w.head_dim * (2 + s) + 8 * n)
     sample = (f"first {n} of {w.num_seqs} sequences of {w.name} (all {w.num_q_heads} query heads, "
-              f"{int(ctx.sum())} context tokens), scatter + fp64 decode, {runs} run(s) in {total:.2f} s")
+              f"{int(ctx.sum())} context tokens), scatter + fp64 decode, {runs} run(s) in "
+              f"{total:.2f} s on {cores} thread(s)")
     return byts * runs / total / 1e9, cores, sample, total, n
+
+
+def cpu_baseline(w, budget_s: float) -> dict:
+    """The oracle timed on every host core and on one core (about two thirds
+    and one third of the budget), with the CPU model."""
+    v, cores, sample, _, _ = cpu_oracle_run(w, budget_s * 2 / 3)
+    v1, _, sample1, _, _ = cpu_oracle_run(w, budget_s / 3, threads=1)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "value_1core": round(v1, 4), "sample_1core": sample1,
+            "cpu_model": cpu_model()}
 
 
 def run_reference(args):
@@ -264,15 +300,140 @@ def run_reference(args):
         "data": "synthetic, seeded (numpy/torch CPU generators)",
         "config": {"workload": w.name, "batch": w.num_seqs, "q_heads": w.num_q_heads,
                    "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "partition_size": w.partition_size,
-                   "kv_dtype": w.dtype},
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "context_tokens": int(w.context_lens.sum()),
+                   "max_context_len": w.max_context_len, "partition_size": w.partition_size,
+                   "kv_dtype": w.kv_dtype or w.dtype},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_cpu_table(args):
+    """The oracle on every workload at all host cores and at one core (a
+    reported baseline, not a target): one JSON line per workload."""
+    import workloads
+    for name in workloads.NAMES:
+        w = workloads.make(name, seed=args.seed)
+        v, cores, sample, _, _ = cpu_oracle_run(w, args.cpu_budget * 2 / 3)
+        v1, _, sample1, _, _ = cpu_oracle_run(w, args.cpu_budget / 3, threads=1)
+        print(json.dumps({"op": "cpu_table", "workload": name, "dtype": w.dtype, "unit": "GB/s",
+                          "all_cores": {"value": round(v, 4), "cores": cores, "sample": sample},
+                          "one_core": {"value": round(v1, 4), "sample": sample1},
+                          "cpu_model": cpu_model()}), flush=True)
+    return 0
+
+
+class Step:
+    """One workload resident on the device and the calls of its decode step:
+    pa_reshape_and_cache of the new tokens, then pa_decode (or their FP8
+    forms) with a zero-filled workspace allocated once."""
+
+    def __init__(self, pa, w, dev):
+        import torch
+        self.pa, self.w, self.dev = pa, w, dev
+        self.fp8 = w.kv_dtype == "e4m3"
+        self.kc, self.vc = w.k_cache.to(dev), w.v_cache.to(dev)
+        self.key, self.value = w.key.to(dev), w.value.to(dev)
+        self.sm = w.slot_mapping.to(dev)
+        self.q = w.query.to(dev)
+        self.bt = w.block_tables.to(dev)
+        self.cl = w.context_lens.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.maxctx = w.max_context_len
+        self.ps = w.partition_size
+        self.nparts = pa.pa_decode_num_partitions(self.maxctx, self.ps)
+        self.ws = pa.new_decode_workspace(w.num_seqs, w.num_q_heads, w.head_dim, self.maxctx,
+                                          self.ps, device=dev)
+
+    def scatter(self, k_new, v_new, slots, st):
+        w, pa = self.w, self.pa
+        if self.fp8:
+            pa.pa_reshape_and_cache_fp8(k_new, v_new, self.kc, self.vc, slots, w.k_scale,
+                                        w.v_scale, stream=st)
+        else:
+            pa.pa_reshape_and_cache(k_new, v_new, self.kc, self.vc, slots, stream=st)
+
+    def decode(self, qq, tables, lens, st):
+        w, pa = self.w, self.pa
+        if self.fp8:
+            pa.pa_decode_fp8(self.out, qq, self.kc, self.vc, tables, lens, w.scale, w.k_scale,
+                             w.v_scale, self.maxctx, self.ps, workspace=self.ws, stream=st)
+        else:
+            pa.pa_decode(self.out, qq, self.kc, self.vc, tables, lens, w.scale, self.maxctx,
+                         self.ps, workspace=self.ws, stream=st)
+
+    def step(self, st):
+        self.scatter(self.key, self.value, self.sm, st)
+        self.decode(self.q, self.bt, self.cl, st)
+
+    def launches_per_step(self) -> int:
+        """Kernels one step launches: the scatter, the decode kernel, and the
+        reduce kernel when the join does not run inside the decode kernel."""
+        fused = self.nparts <= 32 and self.w.num_seqs * self.w.num_kv_heads <= 65536
+        return 2 + (1 if self.nparts > 1 and not fused else 0)
+
+
+def time_steps(fn, K: int, stream, dev) -> float:
+    """Mean ms of K back-to-back calls of fn, CUDA events only at the ends (an
+    event between kernels drains the GPU and hides the launch overlap)."""
+    import torch
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        fn()
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(stop) / K
+
+
+def time_each(fn, K: int, stream, dev) -> float:
+    """Mean ms of K calls of fn, each bracketed by CUDA events on the stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
+    """Step and decode-call figures of another workload ("name:dtype"), in the
+    same run and on the same stream as the main line."""
+    import torch
+
+    import workloads
+    name, dtype = (spec.split(":") + [None])[:2]
+    w = workloads.make(name, seed=args.seed, **({"dtype": dtype} if dtype else {}))
+    ab = algorithmic_bytes(w)
+    s = Step(pa, w, dev)
+    for _ in range(args.warmup):
+        s.step(stream)
+    torch.cuda.synchronize(dev)
+    ms = time_steps(lambda: s.step(stream), args.steps, stream, dev)
+    dms = time_each(lambda: s.decode(s.q, s.bt, s.cl, stream), args.steps, stream, dev)
+    if pa.pa_device_errors(stream) != 0:
+        raise RuntimeError(f"device error bits raised on {spec}")
+    dec_gbs = ab["decode"] / (dms * 1e-3) / 1e9
+    res = {"workload": w.name, "dtype": w.dtype, "batch": w.num_seqs,
+           "partition_size": w.partition_size, "partitions": s.nparts,
+           "ms_per_step": round(ms, 5),
+           "value": round(ab["step"] / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "hbm_fraction": round(ab["step"] / (ms * 1e-3) / 1e9 / peak, 4),
+           "decode_ms": round(dms, 5), "decode_gbs": round(dec_gbs, 2),
+           "roofline_frac": round(dec_gbs / peak, 4),
+           "decode_tokens_per_s": round(w.num_seqs / (ms * 1e-3), 1),
+           "gpu_launches_per_step": s.launches_per_step()}
+    del s
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args):
@@ -294,78 +455,32 @@ def run_ours(args):
 
     w = make_workload(args)
     ab = algorithmic_bytes(w)
-    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
-    key, value = w.key.to(dev), w.value.to(dev)
-    sm = w.slot_mapping.to(dev)
-    q = w.query.to(dev)
-    bt = w.block_tables.to(dev)
-    cl = w.context_lens.to(dev)
-    out = torch.empty_like(q)
-    maxctx = w.max_context_len
-    ps = w.partition_size
-    nparts = pa.pa_decode_num_partitions(maxctx, ps)
-    ws = torch.empty(max(1, pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
-                                                        maxctx, ps)), dtype=torch.uint8,
-                     device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    fp8 = w.kv_dtype == "e4m3"
-
-    def scatter(k_new, v_new, slots, st):
-        if fp8:
-            pa.pa_reshape_and_cache_fp8(k_new, v_new, kc, vc, slots, w.k_scale, w.v_scale,
-                                        stream=st)
-        else:
-            pa.pa_reshape_and_cache(k_new, v_new, kc, vc, slots, stream=st)
-
-    def decode(qq, tables, lens, st):
-        if fp8:
-            pa.pa_decode_fp8(out, qq, kc, vc, tables, lens, w.scale, w.k_scale, w.v_scale, maxctx,
-                             ps, workspace=ws, stream=st)
-        else:
-            pa.pa_decode(out, qq, kc, vc, tables, lens, w.scale, maxctx, ps, workspace=ws,
-                         stream=st)
-
-    def step():
-        scatter(key, value, sm, stream)
-        decode(q, bt, cl, stream)
+    S = Step(pa, w, dev)
+    fp8 = S.fp8
 
     for _ in range(args.warmup):
-        step()
+        S.step(stream)
     torch.cuda.synchronize(dev)
     if pa.pa_device_errors(stream) != 0:
         raise RuntimeError("device error bits raised during warm-up")
 
     K = args.steps
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    # timed region: K back-to-back steps, events only at its two ends (an
-    # event between kernels drains the GPU and hides the launch overlap)
+    # timed region: K back-to-back steps, events only at its two ends
     with ClockSampler(dev.index) as clk:
-        start.record(stream)
-        for _ in range(K):
-            step()
-        stop.record(stream)
-        torch.cuda.synchronize(dev)
+        step_ms = time_steps(lambda: S.step(stream), K, stream, dev)
     if dist:
         dist.barrier()
-    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
-    ms_per_step = total_ms / K
+    ms_per_step = max_over_ranks(step_ms, dist, dev)
     if pa.pa_device_errors(stream) != 0:
         raise RuntimeError("device error bits raised during the timed steps")
 
     # the dominant kernel's own duration: the same K decode calls, each
     # bracketed by CUDA events on the launch stream
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    for i in range(K):
-        ev[i][0].record(stream)
-        decode(q, bt, cl, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    decode_ms = time_each(lambda: S.decode(S.q, S.bt, S.cl, stream), K, stream, dev)
 
     # spread of the step time: 10 blocks of 5 back-to-back steps (events only
     # at block ends), and single steps after an L2 flush (a 2x-L2 memset, then
@@ -374,15 +489,7 @@ def run_ours(args):
         xs = sorted(xs)
         return xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
 
-    blocks = []
-    for _ in range(10):
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for _ in range(5):
-            step()
-        b1.record(stream)
-        torch.cuda.synchronize(dev)
-        blocks.append(b0.elapsed_time(b1) / 5)
+    blocks = [time_steps(lambda: S.step(stream), 5, stream, dev) for _ in range(10)]
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     flushed = []
     for _ in range(20):
@@ -390,7 +497,7 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             flush.zero_()
         f0.record(stream)
-        step()
+        S.step(stream)
         f1.record(stream)
         torch.cuda.synchronize(dev)
         flushed.append(f0.elapsed_time(f1))
@@ -411,25 +518,16 @@ def run_ours(args):
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             for _ in range(2):
-                scatter(key, value, sm, side)
-                decode(q, bt, cl, side)
+                S.step(side)
         stream.wait_stream(side)
         torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            cs = torch.cuda.current_stream(dev)
-            scatter(key, value, sm, cs)
-            decode(q, bt, cl, cs)
+            S.step(torch.cuda.current_stream(dev))
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize(dev)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(K):
-            graph.replay()
-        g1.record(stream)
-        torch.cuda.synchronize(dev)
-        graph_ms = g0.elapsed_time(g1) / K
+        graph_ms = time_steps(graph.replay, K, stream, dev)
         del graph
     except RuntimeError as e:  # capture unsupported: report without the graph figure
         print(f"graph replay skipped: {e}", file=sys.stderr)
@@ -456,40 +554,37 @@ def run_ours(args):
     for n, t in segs:
         seg_view(hstage, n, t).copy_(t)
     dq, dkey, dval, dsm, dbt, dcl = (seg_view(dstage, n, t) for n, t in segs)
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hout = torch.empty(S.out.shape, dtype=S.out.dtype, pin_memory=True)
     h2d = total
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
         dstage.copy_(hstage, non_blocking=True)
-        scatter(dkey, dval, dsm, stream)
-        decode(dq, dbt, dcl, stream)
-        hout.copy_(out, non_blocking=True)
+        S.scatter(dkey, dval, dsm, stream)
+        S.decode(dq, dbt, dcl, stream)
+        hout.copy_(S.out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
+    e2e_ms = max_over_ranks(time_steps(e2e_step, K, stream, dev), dist, dev)
 
     peak, peak_src = hbm_peak()
     achieved = ab["decode"] / (decode_ms * 1e-3) / 1e9
     value_gbs = job_throughput(world, ab["step"], ms_per_step)
     clocks = clk.summary()
 
+    # the other decode targets, measured in the same run (rank 0, one GPU)
+    extras = []
+    if rank == 0 and world == 1:
+        for spec in (args.extra or []):
+            extras.append(measure_extra(pa, spec, args, dev, stream, peak))
+
     line = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            v, cores, sample, dt, n = cpu_oracle_run(w, args.cpu_budget)
-            cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                   "sample": sample}
-        launches_per_step = 2 + (1 if nparts > 1 else 0)  # scatter, decode, join
+            cpu = cpu_baseline(w, args.cpu_budget)
         line = {
             "metric": METRIC,
             "value": round(value_gbs, 2),
@@ -508,8 +603,8 @@ def run_ours(args):
                        "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                        "block_size": w.block_size, "num_blocks": w.num_blocks,
                        "context_tokens": int(w.context_lens.sum()),
-                       "max_context_len": maxctx, "partition_size": ps,
-                       "partitions": nparts, "kv_dtype": w.kv_dtype or w.dtype,
+                       "max_context_len": S.maxctx, "partition_size": S.ps,
+                       "partitions": S.nparts, "kv_dtype": w.kv_dtype or w.dtype,
                        "accumulate": "f32",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": f"no flush: inputs larger than L2 ({ab['kv'] / 1e6:.0f} MB of KV "
@@ -527,8 +622,11 @@ def run_ours(args):
             "hbm_fraction": round(value_gbs / world / peak, 4),
             "step_stats": step_stats,
             "bytes_per_step": ab,
-            "roofline": {"bound": "hbm", "kernel": "pa_decode (main kernel + LSE reduce), "
-                                                    "K event-bracketed calls after the timed steps",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("pa_decode call (one decode kernel; the LSE join runs in it)"
+                                    if S.launches_per_step() == 2 else
+                                    "pa_decode call (decode kernel + LSE reduce kernel)")
+                         + ", K event-bracketed calls after the timed steps",
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
                          # the committed summaries profile the default launch of each
@@ -541,8 +639,9 @@ def run_ours(args):
             "e2e": {"value": round(job_throughput(world, ab["step"], e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": S.launches_per_step() * K,
             "clocks": clocks,
+            "extra_workloads": extras,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -680,14 +779,27 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of host time for the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("step", "blocks", "prefill"), default="step",
+    ap.add_argument("--op", choices=("step", "blocks", "prefill", "cpu-table"), default="step",
                     help="step: the decode step (default); blocks: copy/swap block bandwidth; "
-                         "prefill: chunked-prefill attention")
+                         "prefill: chunked-prefill attention; cpu-table: the oracle on every "
+                         "workload at all cores and one core")
+    ap.add_argument("--extra", action="append", default=None, metavar="NAME[:DTYPE]",
+                    help="another workload measured in the same run (repeatable); default: "
+                         + ", ".join(DEFAULT_EXTRAS) + " beside the default workload")
+    ap.add_argument("--no-extra", action="store_true", help="measure the main workload only")
     ap.add_argument("--chunk", type=int, default=512, help="prefill chunk (tokens)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.no_extra:
+        args.extra = []
+    elif args.extra is None:
+        plain = (args.workload == DEFAULT_WORKLOAD and args.dtype is None
+                 and args.partition_size is None and args.kv_dtype == "same")
+        args.extra = list(DEFAULT_EXTRAS) if plain else []
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "cpu-table":
+        return run_cpu_table(args)
     if args.op == "blocks":
         return run_block_ops(args)
     if args.op == "prefill":

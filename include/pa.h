@@ -75,6 +75,8 @@ typedef enum pa_dtype {
 #define PA_DEVERR_BAD_LEN   4u   /* a context length was < 0, > max_blocks_per_seq * block_size
                                     or > max_context_len */
 #define PA_DEVERR_TIMEOUT   8u   /* a wait for staged KV data ran past its time limit */
+#define PA_DEVERR_WORKSPACE 16u  /* a split-context join counter in the workspace did not
+                                    start at zero (see pa_decode_workspace_size) */
 
 /*
  * pa_reshape_and_cache -- write each new token's key and value into its slot
@@ -113,12 +115,26 @@ int32_t pa_decode_num_partitions(int32_t max_context_len, int32_t partition_size
  * Bytes of workspace pa_decode needs (0 when it runs as one partition).
  * Layout, P = pa_decode_num_partitions(...), R = num_seqs * num_q_heads,
  * each array starting at a 256-byte aligned offset, in this order:
+ *   counters  uint32 [PA_DECODE_COUNTER_BYTES / 4]  join counters (below)
  *   m  float [R, P]      max over the partition of scale * q.k_j * log2(e)
  *   l  float [R, P]      sum over the partition of 2^(scale*q.k_j*log2(e) - m)
  *   o  float [R, P, head_dim]  the partition's normalised attention output
- * Row r = seq * num_q_heads + head; only partitions p < ceil(ctx / partition_size)
- * of a sequence are written.
+ * Row r = seq * num_q_heads + head.  A sequence's partitions
+ * p < ceil(ctx / partition_size) are written, except that when the join runs
+ * inside the decode kernel (P <= 32 and num_seqs * num_kv_heads <= 65536) a
+ * sequence with a single partition writes its output directly and no partial.
+ *
+ * Join counters: word seq * num_kv_heads + kv_head counts the partitions of
+ * that sequence and KV head that have finished; the last one joins them and
+ * sets the word back to zero.  The counter words must therefore be ZERO the
+ * first time a workspace is used (cudaMemset the first PA_DECODE_COUNTER_BYTES
+ * once after allocating it); every completed pa_decode call leaves them zero
+ * again, for any later shape, since the counters never move and no partial is
+ * ever stored over them.  A counter that is found not to have started at zero
+ * sets PA_DEVERR_WORKSPACE and that row's output is not written.
  */
+#define PA_DECODE_COUNTER_BYTES (256u * 1024u)
+
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                 int32_t max_context_len, int32_t partition_size);
 
@@ -136,8 +152,10 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t h
  * (sequence, KV head) writes out directly; workspace may be NULL.
  * partition_size > 0 (a multiple of 16): the tokens of each sequence are cut
  * into partitions of partition_size, each partition is attended to
- * separately into `workspace` (layout above), and pa_decode_reduce joins them
- * by log-sum-exp on the same stream.
+ * separately into `workspace` (layout above, counter words zero), and the
+ * partitions are joined by log-sum-exp: inside the decode kernel, by the last
+ * partition of each (sequence, KV head) to finish, when there are at most 32
+ * partitions; otherwise by pa_decode_reduce on the same stream.
  * max_context_len must be >= every context_lens[i] (sizes the launch).
  * Pointers (out, query, caches) 16-byte aligned; head_dim in {64, 128};
  * block_size in {16, 32}; num_q_heads / num_kv_heads in 1..8.
@@ -159,9 +177,10 @@ pa_status pa_decode(void *out, const void *query,
  * over the ceil(context_lens[i] / partition_size) partitions of each row
  * (0 partitions: out = 0).  `workspace` holds the partials in the layout of
  * pa_decode_workspace_size for the same num_seqs, num_q_heads, head_dim,
- * max_context_len and partition_size (partition_size > 0).  pa_decode calls
- * this itself when it splits; it is exported so partials from elsewhere can
- * be joined.
+ * max_context_len and partition_size (partition_size > 0); the counter words
+ * are not read.  pa_decode calls this itself when it splits into more
+ * partitions than its kernel joins; it is exported so partials from elsewhere
+ * can be joined.
  */
 pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *context_lens,
                            int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -291,26 +310,31 @@ pa_status pa_swap_blocks(const void *src, void *dst, const int64_t *block_mappin
 
 /*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate
- * device memory.  The pages have no counterpart to this call: it exists for
- * code that may not call cudaMalloc, such as work enqueued while a CUDA graph
- * is being captured, host frameworks that have reserved all device memory for
- * their own KV pool, or latency-critical enqueue paths that cannot afford an
- * allocation's implicit device synchronisation.
+ * device memory.  The pages have no counterpart to this call.  Some callers
+ * of a decode kernel may not call cudaMalloc at all: a serving framework that
+ * has reserved nearly all device memory for its own KV pool and hands none of
+ * it to libraries, a plugin running under a host runtime that owns every
+ * allocation on the device, or a real-time enqueue path that cannot risk the
+ * device-wide synchronisation an allocation may cause.
  *
  * Same arguments and result as pa_decode, without workspace / workspace_bytes:
- * the split-context partials go to a fixed array of PA_STATIC_WORKSPACE_BYTES
- * inside the library (a __device__ variable, so every device that loads the
- * library holds that much memory until the process exits).  The call allocates
- * nothing and calls no allocating routine.
- *  - A shape whose pa_decode_workspace_size exceeds PA_STATIC_WORKSPACE_BYTES
- *    is rejected with PA_ERR_UNSUPPORTED before anything is enqueued.
+ * the split-context partials and join counters go to a fixed array of
+ * PA_STATIC_WORKSPACE_BYTES inside the library (a __device__ variable, so
+ * every device that loads the library holds that much memory until the
+ * process exits).  The call allocates nothing and calls no allocating routine.
+ *  - Arguments are checked as pa_decode checks them, with the same statuses;
+ *    then a shape whose pa_decode_workspace_size exceeds
+ *    PA_STATIC_WORKSPACE_BYTES is rejected with PA_ERR_UNSUPPORTED.  Nothing
+ *    is enqueued in either case.
  *  - The first call on a device looks up that device's copy of the array
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
- *  - Every call on a device shares the one array and it keeps the last call's
- *    contents; no entry needs to start at zero.  Calls whose kernels overlap
- *    on the GPU (different streams, or different host threads, without
- *    ordering between them) race on the array: order them.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents.  Each call that splits clears the join counters it uses
+ *    (cudaMemsetAsync on `stream`, no allocation) before its kernels; nothing
+ *    else needs to start at zero.  Calls whose kernels overlap on the GPU
+ *    (different streams, or different host threads, without ordering between
+ *    them) race on the array: order them.
  */
 #define PA_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 
@@ -344,7 +368,7 @@ pa_status pa_selftest_bounded_wait(void *stream);
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(int32_t status);
 
-/* Library ABI version: 1. */
+/* Library ABI version: 2 (2 added the join counters to the workspace). */
 int32_t pa_version(void);
 
 #ifdef __cplusplus

@@ -26,10 +26,16 @@ __all__ = [
     "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill", "pa_selftest_bounded_wait",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
+    "DEVERR_WORKSPACE", "DECODE_COUNTER_BYTES", "new_decode_workspace",
 ]
 
 PA_FP16, PA_BF16 = 0, 1
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_WORKSPACE = 16
+# Bytes of join counters at the start of a split-context workspace
+# (PA_DECODE_COUNTER_BYTES in include/pa.h); they must be zero when a
+# workspace is first used, and every pa_decode call leaves them zero.
+DECODE_COUNTER_BYTES = 256 * 1024
 _DT = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
 
 _lock = threading.Lock()
@@ -144,13 +150,27 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
                                                 partition_size))
 
 
+def new_decode_workspace(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,
+                         partition_size: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (CUDA uint8 tensor) of pa_decode_workspace_size
+    bytes, at least one byte; its join counters start at zero as pa_decode
+    requires, and every pa_decode call leaves them zero, so it can be reused
+    for any later call it is large enough for."""
+    need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                    partition_size)
+    return torch.zeros(max(1, need), dtype=torch.uint8,
+                       device=device if device is not None else torch.cuda.current_device())
+
+
 def pa_decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
               v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
               scale: float, max_context_len: int, partition_size: int = 0,
               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Paged decode attention into ``out`` [B, Hq, d].  ``workspace`` (a CUDA
-    uint8 tensor of pa_decode_workspace_size bytes) is allocated here with
-    torch when it is needed and not given."""
+    uint8 tensor of at least pa_decode_workspace_size bytes whose first
+    DECODE_COUNTER_BYTES were zero when it was first used, e.g. from
+    new_decode_workspace) is allocated here, zero-filled, with torch when it
+    is needed and not given."""
     dt = k_cache.dtype
     for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
         _cuda(n, t, dt)
@@ -170,7 +190,7 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
     ws_ptr, ws_bytes = 0, 0
     if need:
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+            workspace = torch.zeros(need, dtype=torch.uint8, device=query.device)
         _cuda("workspace", workspace)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check("pa_decode", _load().pa_decode(
@@ -205,11 +225,12 @@ def pa_decode_static_workspace(out: torch.Tensor, query: torch.Tensor, k_cache: 
                                v_cache: torch.Tensor, block_tables: torch.Tensor,
                                context_lens: torch.Tensor, scale: float, max_context_len: int,
                                partition_size: int = 0, stream=None) -> torch.Tensor:
-    """pa_decode for callers that may not allocate device memory (work
-    enqueued during CUDA-graph capture, frameworks that have reserved all
-    device memory, enqueue paths that cannot afford an allocation's device
-    synchronisation): the split-context partials go to a fixed 64 MiB array
-    the library carries, so neither this binding nor the library allocates.
+    """pa_decode for callers that may not allocate device memory (a framework
+    that has reserved nearly all device memory for its own KV pool, a plugin
+    whose host runtime owns every allocation, a real-time enqueue path that
+    cannot risk an allocation's device-wide synchronisation): the
+    split-context partials and join counters go to a fixed 64 MiB array the
+    library carries, so neither this binding nor the library allocates.
     Shapes needing more scratch than that raise PaError (unsupported shape).
     All calls on a device share the array; calls that overlap on the GPU race."""
     L = _load()
@@ -341,7 +362,7 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
     ws_ptr, ws_bytes = 0, 0
     if need:
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+            workspace = torch.zeros(need, dtype=torch.uint8, device=query.device)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     _check("pa_decode_fp8", f(
         out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),

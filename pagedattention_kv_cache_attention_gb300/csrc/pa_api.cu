@@ -55,21 +55,28 @@ struct WsLayout {
   size_t m_off, l_off, o_off, total;
 };
 
+// Split-context workspace: the join counters (PA_DECODE_COUNTER_BYTES, a fixed
+// size so that no partial of any shape ever lands on them), then m, l, o.
 WsLayout workspace_layout(int64_t rows, int64_t parts, int64_t head_dim) {
   WsLayout w;
   const size_t ml = static_cast<size_t>(rows * parts) * sizeof(float);
-  w.m_off = 0;
-  w.l_off = align256(ml);
+  w.m_off = PA_DECODE_COUNTER_BYTES;
+  w.l_off = w.m_off + align256(ml);
   w.o_off = w.l_off + align256(ml);
   w.total = w.o_off + align256(static_cast<size_t>(rows * parts * head_dim) * sizeof(float));
   return w;
 }
 
+// Largest partition count whose join runs inside the decode kernel (by the
+// last CTA of each sequence and KV head to finish); more partitions are
+// joined by pa_decode_reduce_kernel, whose many CTAs share the longer join.
+constexpr int32_t kMaxFusedParts = 32;
+
 }  // namespace
 
 extern "C" {
 
-int32_t pa_version(void) { return 1; }
+int32_t pa_version(void) { return 2; }
 
 const char *pa_status_string(int32_t status) {
   switch (status) {
@@ -132,10 +139,17 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t key_s
                                                                                   : PA_ERR_CUDA;
 }
 
-pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *context_lens,
-                           int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                           int32_t max_context_len, int32_t partition_size, int32_t dtype,
-                           void *stream) {
+}  // extern "C"
+
+namespace {
+
+// pa_decode_reduce with the number of tokens the block table can address:
+// pa_decode passes its table's capacity so that a context length the decode
+// kernel refused is refused here too; the exported call has no table.
+pa_status reduce_impl(void *out, const void *workspace, const int32_t *context_lens,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                      int32_t max_context_len, int32_t partition_size, int32_t dtype,
+                      int64_t table_tokens, void *stream) {
   if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || partition_size <= 0 ||
       !dtype_ok(dtype))
     return PA_ERR_INVALID_ARG;
@@ -160,23 +174,34 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
   a.num_parts = P;
   a.partition_size = partition_size;
   a.max_context_len = max_context_len;
+  a.table_tokens = table_tokens;
   a.err = err;
   return pa::launch_reduce(a, head_dim, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }
 
-}  // extern "C"
+}  // namespace
 
-namespace {
+extern "C" pa_status pa_decode_reduce(void *out, const void *workspace,
+                                      const int32_t *context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t head_dim,
+                                      int32_t max_context_len, int32_t partition_size,
+                                      int32_t dtype, void *stream) {
+  return reduce_impl(out, workspace, context_lens, num_seqs, num_q_heads, head_dim,
+                     max_context_len, partition_size, dtype, INT32_MAX, stream);
+}
 
-pa_status decode_impl(void *out, const void *query, const void *k_cache, const void *v_cache,
-                      const int32_t *block_tables, int32_t max_blocks_per_seq,
-                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                      int64_t num_blocks, float scale, int32_t max_context_len,
-                      int32_t partition_size, void *workspace, size_t workspace_bytes,
-                      int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream) {
+// Every host-side check pa_decode makes before it looks at the workspace, in
+// the same order, so that a caller without a workspace gets the status
+// pa_decode would return for the same arguments.
+int32_t pa::decode_check_args(const void *out, const void *query, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                              float scale, int32_t max_context_len, int32_t partition_size,
+                              int32_t dtype) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_context_len < 0 || partition_size < 0 ||
       !dtype_ok(dtype) || !std::isfinite(scale))
@@ -197,6 +222,25 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
     return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7fffffff)
     return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+namespace {
+
+pa_status decode_impl(void *out, const void *query, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int64_t num_blocks, float scale, int32_t max_context_len,
+                      int32_t partition_size, void *workspace, size_t workspace_bytes,
+                      int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream) {
+  const int32_t st = pa::decode_check_args(
+      out, query, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, max_context_len,
+      partition_size, dtype);
+  if (st != PA_OK || num_seqs == 0) return static_cast<pa_status>(st);
+  const int32_t group = num_q_heads / num_kv_heads;
+  const int64_t pool_rows = num_blocks * num_kv_heads * block_size;
   const int32_t P = num_partitions(max_context_len, partition_size);
   WsLayout w{};
   if (P > 1) {
@@ -204,6 +248,8 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
     if (!workspace || workspace_bytes < w.total || !aligned16(workspace))
       return PA_ERR_INVALID_ARG;
   }
+  const bool fuse = P > 1 && P <= kMaxFusedParts &&
+                    static_cast<int64_t>(num_seqs) * num_kv_heads <= PA_DECODE_COUNTER_BYTES / 4;
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
 
@@ -228,15 +274,18 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
   a.ws_m = P > 1 ? reinterpret_cast<float *>(base + w.m_off) : nullptr;
   a.ws_l = P > 1 ? reinterpret_cast<float *>(base + w.l_off) : nullptr;
   a.ws_o = P > 1 ? reinterpret_cast<float *>(base + w.o_off) : nullptr;
+  a.ws_cnt = P > 1 ? reinterpret_cast<unsigned *>(base) : nullptr;
+  a.fuse_join = fuse ? 1 : 0;
   a.err = err;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   bool map_failed = false;
-  if (pa::launch_decode(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8, st,
+  if (pa::launch_decode(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8, cs,
                         &map_failed) != cudaSuccess)
     return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
-  if (P > 1)
-    return pa_decode_reduce(out, workspace, context_lens, num_seqs, num_q_heads, head_dim,
-                            max_context_len, partition_size, dtype, stream);
+  if (P > 1 && !fuse)
+    return reduce_impl(out, workspace, context_lens, num_seqs, num_q_heads, head_dim,
+                       max_context_len, partition_size, dtype,
+                       static_cast<int64_t>(max_blocks_per_seq) * block_size, stream);
   return PA_OK;
 }
 

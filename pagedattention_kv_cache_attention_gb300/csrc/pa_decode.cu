@@ -83,6 +83,73 @@ template <int D, bool F8> struct Shape {
 // with the swizzle puts them in distinct banks.
 __device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
 
+// Each partition CTA adds kJoinArrive to its (sequence, KV head) counter: after
+// k arrivals both 16-bit halves hold k, so a counter that did not start at zero
+// (a workspace whose counter words were not cleared) is recognised.
+constexpr unsigned kJoinArrive = 0x00010001u;
+
+// Log-sum-exp join of the np partitions of one (sequence, KV head), run by the
+// CTA that finished last: out = sum_p w_p o_p / sum_p w_p, w_p = l_p 2^(m_p - M),
+// M = max_p m_p, for the G query heads of the KV head.  Thread items are
+// 4-element chunks of one head's output; partitions are taken 8 at a time with
+// a running maximum, so every group costs one round trip to L2.  The partials
+// were written by other CTAs of this grid: they are read through L2 (ld.cg).
+template <typename T, int D, int NW>
+__device__ __forceinline__ void join_partitions(const DecodeArgs &a, int seq, int kvh, int np) {
+  constexpr int kQuads = D / 4;
+  constexpr int kGroup = 8;
+  const int G = a.group;
+  for (int item = threadIdx.x; item < G * kQuads; item += NW * 32) {
+    const int h = item / kQuads, c4 = item % kQuads;
+    const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h;
+    const float *mrow = a.ws_m + row * a.num_parts;
+    const float *lrow = a.ws_l + row * a.num_parts;
+    const float *orow = a.ws_o + row * a.num_parts * D + c4 * 4;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < np; p0 += kGroup) {
+      float mp[kGroup], lp[kGroup];
+      float4 op[kGroup];
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        if (p0 + u < np) {
+          mp[u] = __ldcg(mrow + p0 + u);
+          lp[u] = __ldcg(lrow + p0 + u);
+          op[u] = __ldcg(reinterpret_cast<const float4 *>(orow + static_cast<int64_t>(p0 + u) * D));
+        } else {
+          mp[u] = -INFINITY;
+          lp[u] = 0.f;
+          op[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) Mn = fmaxf(Mn, mp[u]);
+      const float ref = Mn == -INFINITY ? 0.f : Mn;  // no token yet: any finite reference
+      const float al = exp2f(M - ref);
+      L *= al;
+      acc.x *= al;
+      acc.y *= al;
+      acc.z *= al;
+      acc.w *= al;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const float wgt = lp[u] * exp2f(mp[u] - ref);
+        L += wgt;
+        acc.x += wgt * op[u].x;
+        acc.y += wgt * op[u].y;
+        acc.z += wgt * op[u].z;
+        acc.w += wgt * op[u].w;
+      }
+      M = Mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const uint2 pk = make_uint2(Elem<T>::pack(acc.x * inv, acc.y * inv),
+                                Elem<T>::pack(acc.z * inv, acc.w * inv));
+    *reinterpret_cast<uint2 *>(static_cast<T *>(a.out) + row * D + c4 * 4) = pk;
+  }
+}
+
 // T: query/output type (and the MMA type); F8: the caches hold FP8 E4M3 codes
 // (T is then fp16), converted exactly to fp16 in registers.  NSUB: 16-token
 // sub-tiles per pipeline step (their MMA chains are independent and share one
@@ -143,6 +210,9 @@ __global__ void __launch_bounds__(NW * 32)
     ctx = 0;
   }
   if (part > 0 && t_begin >= ctx) return;  // partition past the end: nothing to write
+  // partitions of this sequence that have tokens (partition 0 also stands for
+  // an empty context)
+  const int np_seq = ctx > 0 ? (ctx + a.part_tokens - 1) / a.part_tokens : 1;
   const int t_end = min(ctx, t_begin + a.part_tokens);
   const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int n_grp = (n_sub + NSUB - 1) / NSUB;
@@ -486,7 +556,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] *= inv;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h;
-    if (a.num_parts == 1) {
+    if (a.num_parts == 1 || (a.fuse_join && np_seq == 1)) {
       uint4 pk;
       pk.x = Elem<T>::pack(o[0], o[1]);
       pk.y = Elem<T>::pack(o[2], o[3]);
@@ -503,6 +573,28 @@ __global__ void __launch_bounds__(NW * 32)
         a.ws_l[pr] = L;
       }
     }
+  }
+  if (a.fuse_join && np_seq > 1) {
+    // count this partition in; the CTA that completes the count joins them all
+    __threadfence();  // this thread's partials are visible GPU-wide before the count
+    __syncthreads();
+    uint32_t *last_flag = reinterpret_cast<uint32_t *>(wml + NW * 8 * 2);
+    if (threadIdx.x == 0) {
+      unsigned *cnt = a.ws_cnt + static_cast<int64_t>(seq) * a.num_kv_heads + kvh;
+      const unsigned prev = atomicAdd(cnt, kJoinArrive);
+      const unsigned k = prev & 0xffffu;
+      uint32_t last = 0;
+      if ((prev >> 16) != k || k >= static_cast<unsigned>(np_seq)) {
+        atomicOr(a.err, kErrWorkspace);  // the counter did not start at zero
+      } else if (k == static_cast<unsigned>(np_seq - 1)) {
+        last = 1;
+        atomicExch(cnt, 0u);  // every partition has arrived: ready for the next call
+      }
+      __threadfence();
+      *last_flag = last;
+    }
+    __syncthreads();
+    if (*last_flag) join_partitions<T, D, NW>(a, seq, kvh, np_seq);
   }
   grid_launch_dependents();
 }
@@ -522,7 +614,9 @@ __global__ void __launch_bounds__(kReduceRows * 32) pa_decode_reduce_kernel(cons
   if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
   const int seq = static_cast<int>(row / a.num_q_heads);
   int ctx = a.context_lens[seq];
-  if (ctx < 0 || ctx > a.max_context_len) {
+  // the same validity test as the decode kernel, so a length it refused joins
+  // no partitions (none of them were written by this call)
+  if (ctx < 0 || ctx > a.max_context_len || ctx > a.table_tokens) {
     if (lane == 0 && row % a.num_q_heads == 0) atomicOr(a.err, kErrBadLen);
     ctx = 0;
   }
@@ -660,21 +754,13 @@ cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CU
   using Sh = Shape<D, F8>;
   constexpr size_t step = 2 * NSUB * Sh::kTileBytes;
   constexpr size_t smem = 1024 + static_cast<size_t>(NW) * S * step + NW * S * 8;
-  static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 <=
+  static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 + 16 <=
                     static_cast<size_t>(NW) * S * step,
-                "merge buffers must fit in the stage area");
+                "merge buffers and the join flag must fit in the stage area");
   auto kern = pa_decode_kernel<T, D, NW, S, F8, NSUB>;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemLimitOnce smem_limit;
+  const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   return launch_dependent(kern, dim3(a.num_parts, a.num_kv_heads, a.num_seqs), dim3(NW * 32),
                           smem, stream, km, vm, a);
 }

@@ -17,6 +17,7 @@ constexpr unsigned kErrBadBlock = 1u;
 constexpr unsigned kErrBadSlot = 2u;
 constexpr unsigned kErrBadLen = 4u;
 constexpr unsigned kErrTimeout = 8u;
+constexpr unsigned kErrWorkspace = 16u;
 
 // Longest a warp waits for one staged tile before it gives up (ns).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;

@@ -5,9 +5,40 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace pa {
 
 constexpr int kMaxDevices = 64;
+
+// Raises one kernel's dynamic shared-memory limit once per device.  Safe when
+// several host threads make their first call at the same time: the attribute
+// is set under a lock, and later calls only read an atomic flag.  Each
+// launcher keeps one function-local static instance per kernel.
+class SmemLimitOnce {
+ public:
+  template <typename Kern>
+  cudaError_t ensure(Kern kern, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (!done_[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(bytes));
+      if (e != cudaSuccess) return e;
+      done_[dev].store(true, std::memory_order_release);
+    }
+    return cudaSuccess;
+  }
+
+ private:
+  std::atomic<bool> done_[kMaxDevices]{};
+  std::mutex mu_;
+};
 
 struct DecodeArgs {
   void *out;                    // [B, Hq, D] (used when num_parts == 1)
@@ -23,6 +54,8 @@ struct DecodeArgs {
   int part_tokens;              // tokens per partition (>= max_context_len when not split)
   int num_parts;
   float *ws_m, *ws_l, *ws_o;    // split partials (num_parts > 1)
+  unsigned *ws_cnt;             // join counters, one per (sequence, KV head) (num_parts > 1)
+  int fuse_join;                // 1: the last partition CTA of a (sequence, KV head) joins
   unsigned *err;                // device error word
 };
 
@@ -31,6 +64,10 @@ struct ReduceArgs {
   const float *ws_m, *ws_l, *ws_o;
   const int32_t *context_lens;
   int num_seqs, num_q_heads, num_parts, partition_size, max_context_len;
+  // tokens the block table can address (max_blocks_per_seq * block_size); a
+  // longer context is treated as invalid exactly as the decode kernel treats
+  // it (INT32_MAX when the partials do not come from pa_decode)
+  int64_t table_tokens;
   unsigned *err;
 };
 
@@ -101,6 +138,15 @@ cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStrea
 cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,
                            int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
                            bool *map_failed);
+
+// The host-side checks of pa_decode that come before the workspace check;
+// returns a pa_status value (PA_OK when pa_decode would go on to the workspace).
+int32_t decode_check_args(const void *out, const void *query, const void *k_cache,
+                          const void *v_cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
+                          int32_t max_context_len, int32_t partition_size, int32_t dtype);
 
 // One CTA waiting on a barrier nothing completes (the wait-limit self-test).
 cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t stream);

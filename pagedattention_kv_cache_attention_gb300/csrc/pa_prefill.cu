@@ -351,17 +351,9 @@ cudaError_t launch_prefill_t(const PrefillArgs &a, const CUtensorMap &km, const 
                              cudaStream_t stream) {
   constexpr size_t smem = 1024 + static_cast<size_t>(S) * 2 * kTile * D * 2 + 2 * S * 8 + S * 4;
   auto kern = pa_prefill_kernel<T, D, NW, S>;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemLimitOnce smem_limit;
+  const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   const int tpc = NW * 16 / a.group;
   const int tiles = (a.max_q_len + tpc - 1) / tpc;
   return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(NW * 32), smem,

@@ -607,17 +607,9 @@ cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km
   constexpr size_t smem = PairLayout<SK, SV, TILES>::kSmem;
   static_assert(smem <= (TILES == 1 ? 113 : 227) * 1024, "shared memory");
   auto kern = pa_prefill_tc_pair_kernel<T, SK, SV, SPLIT, TILES>;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemLimitOnce smem_limit;
+  const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   const int tpc = TILES * kTcRows / a.group;
   const int tiles = (a.max_q_len + tpc - 1) / tpc;
   return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(pair_threads<TILES>()), smem,

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
-    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 1 ? 0 : 1;}\n')
+    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 2 ? 0 : 1;}\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
                     "-I", os.path.join(ROOT, "include"), str(src)], check=True)
 
@@ -66,10 +66,13 @@ def test_partition_count_and_workspace_size(lib):
     assert pa.pa_decode_num_partitions(513, 512) == 2
     assert pa.pa_decode_num_partitions(131072, 512) == 256
     assert pa.pa_decode_workspace_size(8, 32, 128, 512, 512) == 0
-    # m, l [R, P] and o [R, P, d], each 256-byte aligned
+    # the join counters (a fixed 256 KiB), then m, l [R, P] and o [R, P, d],
+    # each 256-byte aligned
     R, P, d = 8 * 32, 256, 128
     ml = (R * P * 4 + 255) // 256 * 256
-    assert pa.pa_decode_workspace_size(8, 32, 128, 131072, 512) == 2 * ml + R * P * d * 4
+    assert pa.DECODE_COUNTER_BYTES == 256 * 1024
+    assert pa.pa_decode_workspace_size(8, 32, 128, 131072, 512) == (
+        pa.DECODE_COUNTER_BYTES + 2 * ml + R * P * d * 4)
 
 
 def _decode_status(lib, **over):

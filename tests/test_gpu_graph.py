@@ -2,11 +2,17 @@
 cut launch overhead).  Every library call only validates on the host and
 enqueues kernels, so a captured step replayed with new inputs written into the
 captured buffers must give the bit-identical result of the same calls made
-eagerly."""
+eagerly -- and, like every GPU result here, match the fp64 oracle: the
+replayed pools bit for bit (the oracle's scatter), the replayed output within
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle|, for both input sets."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
+
+RTOL, ATOL = 1e-2, 2e-3
 
 pytestmark = pytest.mark.gpu
 
@@ -14,6 +20,34 @@ pytestmark = pytest.mark.gpu
 def bits(t):
     """Raw bits of a cache (its unowned slots hold NaN, which compares unequal)."""
     return t.view(torch.uint8)
+
+
+def oracle_step(w, fp8):
+    """The oracle's pools after the step's scatter, and its fp64 output."""
+    if fp8:
+        kh, vh = w.k_cache.numpy().copy(), w.v_cache.numpy().copy()
+        oracle.reshape_and_cache_fp8(w.key, w.value, kh, vh, w.slot_mapping, w.dtype,
+                                     w.k_scale, w.v_scale)
+    else:
+        kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
+        vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
+        oracle.reshape_and_cache(w.key, w.value, kh, vh, w.slot_mapping)
+    ref = oracle.decode(w.query, kh, vh, w.block_tables, w.context_lens, w.scale, w.dtype,
+                        kv_dtype="e4m3" if fp8 else None, k_scale=w.k_scale, v_scale=w.v_scale)
+    return kh, vh, ref
+
+
+def assert_matches_oracle(static, w, fp8, what):
+    kh, vh, ref = oracle_step(w, fp8)
+    for name, host in (("kc", kh), ("vc", vh)):
+        dev = static[name].cpu()
+        got = (dev.numpy() if fp8 else dev.view(torch.int16).numpy().view(np.uint16))
+        assert np.array_equal(got[:w.num_blocks], host), f"{what}: {name} differs from the oracle"
+    got = static["out"].float().cpu().double().numpy()
+    assert np.isfinite(got).all(), what
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside tolerance, max {err.max():.3g}"
 
 
 @pytest.fixture(scope="module")
@@ -48,9 +82,7 @@ def test_captured_step_replays_bitwise(pa, fp8):
                     sm=w.slot_mapping.to(dev), q=w.query.to(dev), bt=w.block_tables.to(dev),
                     cl=w.context_lens.to(dev), out=torch.empty_like(w.query, device=dev))
 
-    ws = torch.empty(pa.pa_decode_workspace_size(base.num_seqs, base.num_q_heads,
-                                                 base.head_dim, maxctx, ps),
-                     dtype=torch.uint8, device=dev)
+    ws = pa.new_decode_workspace(base.num_seqs, base.num_q_heads, base.head_dim, maxctx, ps)
 
     def step(b, w, stream=None):
         if fp8:
@@ -91,6 +123,7 @@ def test_captured_step_replays_bitwise(pa, fp8):
     out, kc, vc = eager["base"]
     assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16))
     assert torch.equal(bits(static["kc"]), bits(kc)) and torch.equal(bits(static["vc"]), bits(vc))
+    assert_matches_oracle(static, base, fp8, "first replay")
 
     # new inputs in the same buffers, replay
     nb = buffers(other)
@@ -102,3 +135,4 @@ def test_captured_step_replays_bitwise(pa, fp8):
     out, kc, vc = eager["other"]
     assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16))
     assert torch.equal(bits(static["kc"]), bits(kc)) and torch.equal(bits(static["vc"]), bits(vc))
+    assert_matches_oracle(static, other, fp8, "replay with new inputs")

@@ -257,14 +257,71 @@ def test_reduce_alone_against_oracle_partials(pa):
     ws = torch.zeros(size, dtype=torch.uint8)
     R = B * Hq
     ml = (R * P * 4 + 255) // 256 * 256
-    ws[:R * P * 4].view(torch.float32).copy_(torch.from_numpy((m * np.log2(np.e)).astype(np.float32).ravel()))
-    ws[ml:ml + R * P * 4].view(torch.float32).copy_(torch.from_numpy(l.astype(np.float32).ravel()))
-    ws[2 * ml:2 * ml + R * P * d * 4].view(torch.float32).copy_(
+    c0 = pa.DECODE_COUNTER_BYTES          # m, l, o follow the join counters
+    ws[c0:c0 + R * P * 4].view(torch.float32).copy_(
+        torch.from_numpy((m * np.log2(np.e)).astype(np.float32).ravel()))
+    ws[c0 + ml:c0 + ml + R * P * 4].view(torch.float32).copy_(
+        torch.from_numpy(l.astype(np.float32).ravel()))
+    ws[c0 + 2 * ml:c0 + 2 * ml + R * P * d * 4].view(torch.float32).copy_(
         torch.from_numpy(o.astype(np.float32).ravel()))
     out = torch.empty(B, Hq, d, dtype=torch.float16, device="cuda")
     pa.pa_decode_reduce(out, ws.cuda(), w.context_lens.cuda(), w.max_context_len, ps)
     got = out.float().cpu().double().numpy()
     assert_close(got, ref.reshape(B, Hq, d), "reduce")
+
+
+def test_join_counters_return_to_zero_across_shapes(pa):
+    """Split calls joined inside the decode kernel (at most 32 partitions) leave
+    the workspace's counter words zero, so one zero-filled workspace serves
+    successive calls of different shapes; every output matches the oracle."""
+    cases = [(W.make("llama3_8b_gqa", 31, lens=[900, 1500, 300, 2000]), 512),
+             (W.make("llama3_70b_cb", 32, lens=[1, 700, 64, 65, 2000, 33]), 64),
+             (W.make("tiny_mha", 33, lens=[0, 17, 200, 99]), 16),
+             (W.make("llama3_8b_gqa", 34, lens=[4000, 10, 512, 513], dtype="bf16"), 128)]
+    need = max(pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
+                                           w.max_context_len, ps) for w, ps in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for w, ps in cases:
+            P = pa.pa_decode_num_partitions(w.max_context_len, ps)
+            assert 1 < P <= 32
+            run = Run(pa, w, partition_sizes=[])
+            out = torch.empty_like(run.q)
+            pa.pa_decode(out, run.q, run.kc, run.vc, run.bt, run.cl, w.scale, w.max_context_len,
+                         ps, workspace=ws)
+            torch.cuda.synchronize()
+            assert pa.pa_device_errors() == 0
+            assert int(ws[:pa.DECODE_COUNTER_BYTES].count_nonzero()) == 0
+            run.outs = {ps: out}
+            check_decode(run)
+
+
+def test_join_counter_not_zero_is_flagged(pa):
+    """A workspace whose counter words were not cleared is reported as
+    PA_DEVERR_WORKSPACE, without a fault; a sequence short enough for one
+    partition is still exact (it never uses a counter); once the counters are
+    cleared, the same call matches the oracle."""
+    w = W.make("llama3_8b_gqa", 35, lens=[900, 1500, 300])
+    ps = 512
+    run = Run(pa, w, partition_sizes=[])
+    size = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim,
+                                       w.max_context_len, ps)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    ws[:4 * w.num_seqs * w.num_kv_heads].view(torch.int32).fill_(5)
+    out = torch.zeros_like(run.q)
+    pa.pa_decode(out, run.q, run.kc, run.vc, run.bt, run.cl, w.scale, w.max_context_len, ps,
+                 workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() & pa.DEVERR_WORKSPACE
+    kh, vh = run.host_pool()
+    ref = oracle.decode(w.query, kh, vh, w.block_tables, w.context_lens, w.scale, w.dtype)
+    assert_close(out[2:].float().cpu().double().numpy(), ref[2:], "one-partition sequence")
+    ws.zero_()
+    pa.pa_decode(out, run.q, run.kc, run.vc, run.bt, run.cl, w.scale, w.max_context_len, ps,
+                 workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() == 0
+    assert_close(out.float().cpu().double().numpy(), ref, "after clearing the counters")
 
 
 # ------------------------------------------------------------ device errors
