@@ -184,11 +184,23 @@ def job_throughput(world: int, bytes_per_step: int, ms_per_step: float) -> float
     return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
-def make_workload(args):
-    import workloads
+def shape_overrides(args) -> dict:
+    """Workload keyword overrides from the command line (dtype and head shape)."""
     kw = {}
     if args.dtype:
         kw["dtype"] = args.dtype
+    if args.head_dim:
+        kw["head_dim"] = args.head_dim
+    if args.q_heads:
+        kw["num_q_heads"] = args.q_heads
+    if args.kv_heads:
+        kw["num_kv_heads"] = args.kv_heads
+    return kw
+
+
+def make_workload(args):
+    import workloads
+    kw = shape_overrides(args)
     if args.partition_size is not None:
         kw["partition_size"] = args.partition_size
     w = workloads.make(args.workload, seed=args.seed, **kw)
@@ -631,7 +643,8 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4),
                          # the committed summaries profile the default launch of each
                          # workload (its own dtype and partition size, 16-bit cache)
-                         "traffic": (profiled_traffic(w.name) if not fp8 and args.dtype is None
+                         "traffic": (profiled_traffic(w.name) if not fp8
+                                     and not shape_overrides(args)
                                      and args.partition_size is None else None),
                          "peak_source": peak_src,
                          "decode_ms": round(decode_ms, 5)},
@@ -732,8 +745,8 @@ def run_prefill(args):
     import pagedattention_kv_cache_attention_gb300 as pa
     import workloads
     dev = torch.device("cuda", 0)
-    kw = dict(dtype=args.dtype) if args.dtype else {}
-    pw = workloads.make_prefill(args.workload, seed=args.seed, chunk=args.chunk, **kw)
+    pw = workloads.make_prefill(args.workload, seed=args.seed, chunk=args.chunk,
+                                **shape_overrides(args))
     kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
     key, value, sm = pw.key.to(dev), pw.value.to(dev), pw.slot_mapping.to(dev)
     q, qs = pw.query.to(dev), pw.query_start.to(dev)
@@ -758,6 +771,7 @@ def run_prefill(args):
     fl = prefill_flops(pw)
     print(json.dumps({"op": "prefill", "workload": pw.name, "chunk": args.chunk,
                       "seqs": pw.num_seqs, "total_q": pw.total_q, "dtype": pw.dtype,
+                      "head_dim": pw.head_dim, "group": pw.num_q_heads // pw.num_kv_heads,
                       "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "tokens_per_s": round(pw.total_q / (ms * 1e-3), 1)}), flush=True)
     return 0
@@ -788,12 +802,15 @@ def main(argv=None):
                          + ", ".join(DEFAULT_EXTRAS) + " beside the default workload")
     ap.add_argument("--no-extra", action="store_true", help="measure the main workload only")
     ap.add_argument("--chunk", type=int, default=512, help="prefill chunk (tokens)")
+    ap.add_argument("--head-dim", type=int, default=None, help="override the workload's head_dim")
+    ap.add_argument("--q-heads", type=int, default=None, help="override the query head count")
+    ap.add_argument("--kv-heads", type=int, default=None, help="override the KV head count")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.no_extra:
         args.extra = []
     elif args.extra is None:
-        plain = (args.workload == DEFAULT_WORKLOAD and args.dtype is None
+        plain = (args.workload == DEFAULT_WORKLOAD and not shape_overrides(args)
                  and args.partition_size is None and args.kv_dtype == "same")
         args.extra = list(DEFAULT_EXTRAS) if plain else []
     if args.impl == "reference":

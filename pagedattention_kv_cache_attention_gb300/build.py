@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpa.so")
-SOURCES = ("pa_api.cu", "pa_blocks.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill.cu",
-           "pa_prefill_tc.cu", "pa_static_ws.cu")
+SOURCES = ("pa_api.cu", "pa_blocks.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill_tc.cu",
+           "pa_static_ws.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

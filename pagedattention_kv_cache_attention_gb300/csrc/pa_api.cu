@@ -404,7 +404,6 @@ pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
   a.num_blocks = num_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = err;
-  a.use_tc = true;
   bool map_failed = false;
   if (pa::launch_prefill(a, k_cache, v_cache, pool_rows, head_dim, dtype,
                          static_cast<cudaStream_t>(stream), &map_failed) != cudaSuccess)

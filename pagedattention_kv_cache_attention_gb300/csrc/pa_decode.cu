@@ -83,6 +83,14 @@ template <int D, bool F8> struct Shape {
 // with the swizzle puts them in distinct banks.
 __device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Each partition CTA adds kJoinArrive to its (sequence, KV head) counter: after
 // k arrivals both 16-bit halves hold k, so a counter that did not start at zero
 // (a workspace whose counter words were not cleared) is recognised.
@@ -575,13 +583,15 @@ __global__ void __launch_bounds__(NW * 32)
     }
   }
   if (a.fuse_join && np_seq > 1) {
-    // count this partition in; the CTA that completes the count joins them all
-    __threadfence();  // this thread's partials are visible GPU-wide before the count
+    // count this partition in; the CTA that completes the count joins them
+    // all.  The barrier orders every thread's partial stores before thread 0's
+    // acquire-release add, which publishes them (release, cumulative) and, for
+    // the last CTA, makes every other CTA's partials visible (acquire).
     __syncthreads();
     uint32_t *last_flag = reinterpret_cast<uint32_t *>(wml + NW * 8 * 2);
     if (threadIdx.x == 0) {
       unsigned *cnt = a.ws_cnt + static_cast<int64_t>(seq) * a.num_kv_heads + kvh;
-      const unsigned prev = atomicAdd(cnt, kJoinArrive);
+      const unsigned prev = atom_add_acq_rel_gpu(cnt, kJoinArrive);
       const unsigned k = prev & 0xffffu;
       uint32_t last = 0;
       if ((prev >> 16) != k || k >= static_cast<unsigned>(np_seq)) {
@@ -590,7 +600,6 @@ __global__ void __launch_bounds__(NW * 32)
         last = 1;
         atomicExch(cnt, 0u);  // every partition has arrived: ready for the next call
       }
-      __threadfence();
       *last_flag = last;
     }
     __syncthreads();

@@ -96,7 +96,6 @@ struct PrefillArgs {
   int64_t num_blocks;
   float scale_log2;
   unsigned *err;
-  bool use_tc;                  // allow the tcgen05 kernel where it applies
 };
 
 struct BlockCopyArgs {

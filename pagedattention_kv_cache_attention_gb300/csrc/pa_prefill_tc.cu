@@ -3,11 +3,11 @@
 //
 // Same computation as pa_prefill.cu ("Serving engines", How vLLM works:
 // chunked prefill; chunk row t at position ctx - q_len + t attends causally to
-// tokens 0..t's position through the block table), for head_dim 128 and query
-// groups G in {1, 2, 4, 8}.  One kernel template, two shapes: two 128-row
-// query tiles per CTA (one CTA per SM) for chunks longer than 128/G tokens,
-// one tile per CTA (two CTAs per SM) for shorter ones.  The design and the
-// measurements that shaped it are described above the kernel.
+// tokens 0..t's position through the block table), for head_dim 64 or 128 and
+// every query group G from 1 to 8.  One kernel template, two shapes: two
+// 128-row query tiles per CTA (one CTA per SM) for chunks longer than 128/G
+// tokens, one tile per CTA (two CTAs per SM) for shorter ones.  The design and
+// the measurements that shaped it are described above the kernel.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -23,8 +23,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kTcRows = 128;     // query rows per CTA = TMEM lanes
-constexpr int kTcDim = 128;      // head_dim
+constexpr int kTcRows = 128;     // query rows per tile = TMEM lanes
 constexpr float kRescaleLog2 = 8.f;         // move the running max only past this growth
 constexpr unsigned kFullMask = 0xffffffffu;
 
@@ -80,12 +79,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // Query tiles per CTA, 64-key steps, scores and P in separate TMEM columns.
 //
 // A CTA holds TILES (1 or 2) 128-row tiles of the same (sequence, KV head) --
-// 128 TILES rows = 128 TILES / G tokens x G heads -- and streams 64-key K/V
-// steps through two rings shared by its tiles (K and V apart, so a K stage is
-// refilled as soon as the Q K^T products that read it are done).  Each tile
-// owns 256 TMEM columns: scores (64, fp32), P (64: two 32-column fp16 buffers,
-// or one bf16 buffer of hi + lo parts) and O (128).  Two tiles take all 512
-// columns and one CTA per SM; one tile takes 256 and two CTAs share an SM.
+// rows r = token (r / G) x head (r % G) of floor(128 TILES / G) tokens; when G
+// does not divide 128 a token's heads may straddle the two tiles and the last
+// 128 TILES mod G rows stay idle -- and streams 64-key K/V steps through two
+// rings shared by its tiles (K and V apart, so a K stage is refilled as soon
+// as the Q K^T products that read it are done).  Each tile owns 256 TMEM
+// columns: scores (64, fp32), P (64: two 32-column fp16 buffers, or one bf16
+// buffer of hi + lo parts) and O (head_dim, 64 or 128).  Two tiles take all
+// 512 columns and one CTA per SM; one tile takes 256 and two CTAs share an SM.
+// Q, K and V are staged as 64-dimension atoms of 128-byte rows (one atom at
+// head_dim 64, two at 128).
 // The softmax warps release the score columns as soon as they have loaded
 // them, so Q K^T of step n + 1 runs while they work on step n, and P V of step
 // n runs while they work on step n + 1.  Q is read from shared memory (one
@@ -110,28 +113,31 @@ constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V st
 template <int TILES>
 constexpr int pair_threads() { return 32 * (6 * TILES + 2); }
 
-template <int SK, int SV, int TILES>
+template <int SK, int SV, int TILES, int D>
 struct PairLayout {
-  static constexpr int kQOff = 0;                              // Q: [TILES][2 atoms]
-  static constexpr int kKOff = TILES * 2 * kPairQAtom;         // K ring: [SK][2 atoms]
-  static constexpr int kVOff = kKOff + SK * 2 * kPairKvAtom;   // V ring: [SV][2 atoms]
-  static constexpr int kBarOff = kVOff + SV * 2 * kPairKvAtom;
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kQOff = 0;                                   // Q: [TILES][atoms]
+  static constexpr int kKOff = TILES * kAtoms * kPairQAtom;         // K ring: [SK][atoms]
+  static constexpr int kVOff = kKOff + SK * kAtoms * kPairKvAtom;   // V ring: [SV][atoms]
+  static constexpr int kBarOff = kVOff + SV * kAtoms * kPairKvAtom;
   static constexpr int kBars = 2 * SK + 2 * SV + 1 + 2 + 2 + 4 + 4 + 1;
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
 };
 
-template <typename T, int SK, int SV, bool SPLIT, int TILES>
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES>
 __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
-  using L = PairLayout<SK, SV, TILES>;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  using L = PairLayout<SK, SV, TILES, D>;
+  constexpr int kAtoms = L::kAtoms;
   constexpr int kIssue0 = 4 * TILES;      // first MMA-issuing warp
   constexpr int kLoad0 = 6 * TILES;       // K producer warp (V: kLoad0 + 1)
   constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
-  // TMEM columns of a tile: scores 0..63, P 64..127, O 128..255.  fp16 P: two
+  // TMEM columns of a tile: scores 0..63, P 64..127, O from 128.  fp16 P: two
   // buffers of 32 columns (step n in buffer n % 2); bf16 P: one buffer, hi
   // parts in 64..95 and lo parts in 96..127.
   constexpr int kPBufs = SPLIT ? 1 : 2;
@@ -199,10 +205,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   const int t_last = min(q_len, t_first + tpc) - 1;
   const int base_pos = ctx - q_len;
   // per tile: last token (-1 when the tile has no rows) and step count; tile 1
-  // holds the later tokens, so it reads every step tile 0 reads
-  const int half = kTcRows / G;
-  const int last0 = min(t_last, t_first + half - 1);
-  const int last1 = TILES == 2 && t_first + half <= t_last ? t_last : -1;
+  // holds the later tokens, so it reads every step tile 0 reads.  Tile 0's
+  // rows reach token (kTcRows - 1) / G; tile 1's begin at token kTcRows / G.
+  const int last0 = min(t_last, t_first + (kTcRows - 1) / G);
+  const int last1 = TILES == 2 && t_first + kTcRows / G <= t_last ? t_last : -1;
   const int n_keys = base_pos + t_last + 1;
   const int n_steps0 = active ? (base_pos + last0 + 1 + kPairKeys - 1) / kPairKeys : 0;
   const int n_steps1 = active && last1 >= 0 ? (n_keys + kPairKeys - 1) / kPairKeys : 0;
@@ -222,10 +228,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     {
       const T *qrow = static_cast<const T *>(a.query) +
                       (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
-                       rc % G) * kTcDim;
-      uint8_t *qt = smem + L::kQOff + t * 2 * kPairQAtom;
+                       rc % G) * D;
+      uint8_t *qt = smem + L::kQOff + t * kAtoms * kPairQAtom;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < D / 8; ++ch) {
         const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
                                : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(qt + (ch >> 3) * kPairQAtom + r * 128 +
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < D / 32; ++cb) {
           float o[32];
           tmem_ld32(lane_addr + kOCol + cb * 32, o);
           tmem_wait_ld();
@@ -379,9 +385,9 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T *orow = static_cast<T *>(a.out) +
-                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G) * kTcDim;
+                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G) * D;
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < D / 32; ++cb) {
           float o[32];
           tmem_ld32(lane_addr + kOCol + cb * 32, o);
           tmem_wait_ld();
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       bool ok_run = true;
       if (qk_role) {
         const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
-        const uint32_t qb = smem_addr(smem + L::kQOff) + t * 2 * kPairQAtom;
+        const uint32_t qb = smem_addr(smem + L::kQOff) + t * kAtoms * kPairQAtom;
         const uint32_t sk0 = smem_addr(smem + L::kKOff);
         ok_run = mbar_wait_bounded(q_ready, 0);
         for (int n = 0; n < nt && ok_run; ++n) {
@@ -426,9 +432,9 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
             break;
           }
           tc_fence_after();
-          const uint32_t kb = sk0 + (n % SK) * 2 * kPairKvAtom;
+          const uint32_t kb = sk0 + (n % SK) * kAtoms * kPairKvAtom;
 #pragma unroll
-          for (int k = 0; k < kTcDim / 16; ++k) {
+          for (int k = 0; k < D / 16; ++k) {
             const uint64_t da = umma_desc_sw128(qb + (k >> 2) * kPairQAtom + (k & 3) * 32, 16, 1024);
             const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kPairKvAtom + (k & 3) * 32, 16, 1024);
             umma_f16(tt, da, db, id_qk, k > 0);
@@ -444,7 +450,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
           mbar_arrive(&k_empty[m % SK]);
         }
       } else {
-        const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, kTcDim);
+        const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, D);
         const uint32_t sv0 = smem_addr(smem + L::kVOff);
         for (int n = 0; n < nt && ok_run; ++n) {
           const int s = n % SV, pb = n % kPBufs;
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
             break;
           }
           tc_fence_after();
-          const uint32_t vb = sv0 + s * 2 * kPairKvAtom;
+          const uint32_t vb = sv0 + s * kAtoms * kPairKvAtom;
 #pragma unroll
           for (int kk = 0; kk < kPairKeys / 16; ++kk) {
             const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kPairKvAtom, 1024);
@@ -503,13 +509,13 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       // lane h < kSub issues the copies of sub-tile h
       const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
       const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
-      const uint32_t bytes = __popc(mask) * 2 * 2048;
+      const uint32_t bytes = __popc(mask) * kAtoms * 2048;
       auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
         if (lane < kSub && my_phys >= 0) {
           const int u = n * kSub + lane;
           const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
+          for (int b = 0; b < kAtoms; ++b)
             tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
         }
       };
@@ -528,12 +534,12 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
         if (!ok_run) break;
         __syncwarp();
-        load(smem + L::kKOff + sk * 2 * kPairKvAtom, &kmap, &k_full[sk]);
+        load(smem + L::kKOff + sk * kAtoms * kPairKvAtom, &kmap, &k_full[sk]);
         continue;
       }
       // V: rows past the keys in use and sub-tiles not loaded become zeros
       const int sv = n % SV;
-      uint8_t *vst = smem + L::kVOff + sv * 2 * kPairKvAtom;
+      uint8_t *vst = smem + L::kVOff + sv * kAtoms * kPairKvAtom;
       if (lane == 0 && n >= SV && !mbar_wait_bounded(&v_empty[sv], ((n / SV) - 1) & 1))
         ok_run = false;
       ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
@@ -542,9 +548,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       const int key0 = n * kPairKeys;
       const bool tail = key0 + kPairKeys > n_keys;
       if (mask != kAllSub) {
-        // sub-tiles with no load: zero both 64-dim atoms of their 16 rows
-        for (int i = lane; i < kSub * 2 * 16 * 8; i += 32) {  // 16-byte units
-          const int h = i >> 8, b = (i >> 7) & 1, row = (i >> 3) & 15, u16 = i & 7;
+        // sub-tiles with no load: zero every 64-dim atom of their 16 rows
+        for (int i = lane; i < kSub * kAtoms * 16 * 8; i += 32) {  // 16-byte units
+          const int h = i / (kAtoms * 128), b = (i >> 7) % kAtoms, row = (i >> 3) & 15,
+                    u16 = i & 7;
           if (!((mask >> h) & 1u))
             *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + (h * 16 + row) * 128 + u16 * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -575,8 +582,8 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         }
         __syncwarp();
         const int first = n_keys - key0;  // first row to clear
-        for (int i = lane; i < kPairKeys * 2 * 8; i += 32) {
-          const int row = i >> 4, b = (i >> 3) & 1, u16 = i & 7;
+        for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {
+          const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
           if (row >= first)
             *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + row * 128 + u16 * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -601,12 +608,12 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   grid_launch_dependents();
 }
 
-template <typename T, int SK, int SV, bool SPLIT, int TILES>
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES>
 cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km,
                                      const CUtensorMap &vm, cudaStream_t stream) {
-  constexpr size_t smem = PairLayout<SK, SV, TILES>::kSmem;
+  constexpr size_t smem = PairLayout<SK, SV, TILES, D>::kSmem;
   static_assert(smem <= (TILES == 1 ? 113 : 227) * 1024, "shared memory");
-  auto kern = pa_prefill_tc_pair_kernel<T, SK, SV, SPLIT, TILES>;
+  auto kern = pa_prefill_tc_pair_kernel<T, D, SK, SV, SPLIT, TILES>;
   static SmemLimitOnce smem_limit;
   const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
@@ -632,27 +639,51 @@ cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km
 #endif
 
 bool prefill_tc_supported(int head_dim, int group) {
-  return head_dim == kTcDim && (group == 1 || group == 2 || group == 4 || group == 8);
+  return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= 8;
 }
 
-// Chunks that fill more than one 128-row tile run with two tiles per CTA (one
-// CTA per SM); shorter ones (short chunks, decode-like rows) with one tile per
-// CTA, two CTAs per SM.
-cudaError_t launch_prefill_tc(const PrefillArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
-                              int dtype, cudaStream_t stream) {
+namespace {
+
+template <int D>
+cudaError_t launch_prefill_tc_d(const PrefillArgs &a, const CUtensorMap &km,
+                                const CUtensorMap &vm, int dtype, cudaStream_t stream) {
   const bool pair = static_cast<int64_t>(a.max_q_len) * a.group > kTcRows;
   if (dtype == 0) {
     if (pair)
-      return launch_prefill_tc_pair_t<__half, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
+      return launch_prefill_tc_pair_t<__half, D, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
                                       false, 2>(a, km, vm, stream);
-    return launch_prefill_tc_pair_t<__half, PA_PREFILL_SOLO_KSTAGES, PA_PREFILL_SOLO_VSTAGES, false,
-                                    1>(a, km, vm, stream);
+    return launch_prefill_tc_pair_t<__half, D, PA_PREFILL_SOLO_KSTAGES, PA_PREFILL_SOLO_VSTAGES,
+                                    false, 1>(a, km, vm, stream);
   }
   if (pair)
-    return launch_prefill_tc_pair_t<__nv_bfloat16, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
-                                    true, 2>(a, km, vm, stream);
-  return launch_prefill_tc_pair_t<__nv_bfloat16, PA_PREFILL_SOLO_KSTAGES, PA_PREFILL_SOLO_VSTAGES,
-                                  true, 1>(a, km, vm, stream);
+    return launch_prefill_tc_pair_t<__nv_bfloat16, D, PA_PREFILL_PAIR_KSTAGES,
+                                    PA_PREFILL_PAIR_VSTAGES, true, 2>(a, km, vm, stream);
+  return launch_prefill_tc_pair_t<__nv_bfloat16, D, PA_PREFILL_SOLO_KSTAGES,
+                                  PA_PREFILL_SOLO_VSTAGES, true, 1>(a, km, vm, stream);
+}
+
+}  // namespace
+
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
+                     bool fp8);
+
+// Every shape pa_prefill accepts runs here.  Chunks that fill more than one
+// 128-row tile run with two tiles per CTA (one CTA per SM); shorter ones
+// (short chunks, decode-like rows) with one tile per CTA, two CTAs per SM.
+cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,
+                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                           bool *map_failed) {
+  CUtensorMap km, vm;
+  *map_failed = false;
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, false) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, false)) {
+    *map_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  if (a.max_q_len == 0) return cudaSuccess;
+  if (!prefill_tc_supported(head_dim, a.group)) return cudaErrorInvalidValue;
+  return head_dim == 128 ? launch_prefill_tc_d<128>(a, km, vm, dtype, stream)
+                         : launch_prefill_tc_d<64>(a, km, vm, dtype, stream);
 }
 
 }  // namespace pa

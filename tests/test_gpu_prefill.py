@@ -64,6 +64,18 @@ CASES = [
     ("llama3_8b_gqa", dict(lens=[500, 64], chunk=50, num_q_heads=16, num_kv_heads=8,
                            dtype="bf16")),                                  # G = 2, one-tile kernel
     ("llama3_70b_cb", dict(lens=[700, 1200], chunk=150, dtype="bf16")),     # G = 8, bf16, bs 32
+    # groups that do not divide 128 (a token's heads straddle the two tiles)
+    ("llama3_70b_cb", dict(lens=[400, 900, 61], chunk=140, num_q_heads=40, num_kv_heads=8)),  # G = 5
+    ("llama3_70b_cb", dict(lens=[333, 129], chunk=10**6, num_q_heads=48, num_kv_heads=8,
+                           dtype="bf16")),                                                   # G = 6
+    ("llama3_8b_gqa", dict(lens=[260, 45, 700], chunk=37, num_q_heads=28, num_kv_heads=4)),  # G = 7
+    ("llama3_8b_gqa", dict(lens=[1000, 18], chunk=15, num_q_heads=24, num_kv_heads=8,
+                           head_dim=64)),                                    # G = 3, d 64, one tile
+    # head_dim 64 on both tile shapes
+    ("llama3_8b_gqa", dict(lens=[900, 300, 1700], chunk=256, head_dim=64)),              # G = 4
+    ("llama3_8b_gqa", dict(lens=[500, 64], chunk=20, head_dim=64, dtype="bf16")),        # one tile
+    ("llama3_70b_cb", dict(lens=[800, 33], chunk=100, head_dim=64, num_q_heads=56,
+                           num_kv_heads=8)),                                             # G = 7, d 64
 ]
 
 
@@ -128,8 +140,8 @@ def test_prefill_bench_size_repeatable(pa, dtype):
         assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
 
 
-@pytest.mark.parametrize("chunk,head_dim", [(300, 128), (20, 128), (40, 64)],
-                         ids=["two-tile", "one-tile", "mma-sync"])
+@pytest.mark.parametrize("chunk,head_dim", [(300, 128), (20, 128), (40, 64), (10, 64)],
+                         ids=["two-tile", "one-tile", "two-tile-d64", "one-tile-d64"])
 def test_prefill_bad_block_flagged_others_exact(pa, chunk, head_dim):
     """An out-of-range block id in one sequence's table: the call flags it,
     reads nothing through it (that sequence's rows stay finite), and every
@@ -162,19 +174,20 @@ def test_prefill_bad_block_flagged_others_exact(pa, chunk, head_dim):
 
 def _random_case(i):
     """Seeded random prefill shape: batch 1-4, contexts up to 1500, chunk 1-600,
-    group 1/2/4/8 at head_dim 128 (both tcgen05 kernels), block size 16 or 32,
+    group 1-8, head_dim 64 or 128 (both tile shapes), block size 16 or 32,
     fp16 or bf16."""
     rng = np.random.default_rng(1000 + i)
-    G = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.integers(1, 9))
     hkv = int(rng.choice([1, 2, 4]))
     batch = int(rng.integers(1, 5))
     lens = [int(x) for x in rng.integers(1, 1501, batch)]
     chunk = int(rng.choice([1, 7, 33, 64, 100, 257, 600]))
     return dict(lens=lens, chunk=chunk, num_q_heads=G * hkv, num_kv_heads=hkv,
-                block_size=int(rng.choice([16, 32])), dtype=str(rng.choice(["fp16", "bf16"])))
+                head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([16, 32])),
+                dtype=str(rng.choice(["fp16", "bf16"])))
 
 
-@pytest.mark.parametrize("i", range(40))
+@pytest.mark.parametrize("i", range(48))
 def test_prefill_random_shapes(pa, i):
     pw = W.make_prefill("llama3_8b_gqa", 70 + i, **_random_case(i))
     kc, vc, out, err = run(pa, pw)
