@@ -786,7 +786,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dtype", choices=("fp16", "bf16"), default=None)
     ap.add_argument("--kv-dtype", choices=("same", "e4m3"), default="same",
-                    help="e4m3: FP8 KV cache (fp16 queries)")
+                    help="e4m3: FP8 KV cache (16-bit queries)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=None,
                     help="override the workload's split-context partition (tokens, 0 = none)")

@@ -249,9 +249,13 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
 /*
  * pa_decode_fp8 -- pa_decode over FP8 caches: K_j = k_scale * e4m3(k code),
  * V_j = v_scale * e4m3(v code).  Codes are converted exactly to fp16 in the
- * kernel; k_scale joins the softmax scale and v_scale multiplies the output.
- * query/out fp16 (dtype = PA_FP16; PA_BF16 returns PA_ERR_UNSUPPORTED),
- * head_dim 128, block_size 16 or 32.  Workspace as for pa_decode.
+ * kernel and both products run in fp16 with fp32 accumulation; k_scale joins
+ * the softmax scale and v_scale multiplies the output.  query/out fp16
+ * (dtype = PA_FP16) or bf16 (PA_BF16): bf16 queries are scaled by a power of
+ * two per (sequence, KV head) so that their largest magnitude fits fp16, then
+ * rounded to fp16 (exact for every value down to 2^-31 of the largest), and
+ * the power of two is taken back out of the softmax scale.  head_dim 128,
+ * block_size 16 or 32.  Workspace as for pa_decode.
  */
 pa_status pa_decode_fp8(void *out, const void *query,
                         const void *k_cache, const void *v_cache,

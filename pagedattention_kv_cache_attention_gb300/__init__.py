@@ -342,7 +342,7 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
                   partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
                   stream=None) -> torch.Tensor:
     """Paged decode attention over uint8 FP8 E4M3 caches (codes times
-    k_scale / v_scale) into ``out`` [B, Hq, d] (fp16 queries and output)."""
+    k_scale / v_scale) into ``out`` [B, Hq, d] (fp16 or bf16 queries and output)."""
     P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     f = _blocks_fn("pa_decode_fp8", [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f32,
                                      f32, f32, i32, i32, P, sz, i32, P])

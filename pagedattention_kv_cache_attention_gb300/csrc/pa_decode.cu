@@ -52,6 +52,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -167,7 +168,11 @@ __global__ void __launch_bounds__(NW * 32)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<D, F8>;
-  static_assert(!F8 || (D == 128 && sizeof(T) == 2), "FP8 caches: head_dim 128, fp16 queries");
+  static_assert(!F8 || (D == 128 && sizeof(T) == 2), "FP8 caches: head_dim 128, 16-bit queries");
+  // MMA operand type: the query type, except over FP8 caches, whose codes are
+  // exact in fp16 (and not all in bf16's exponent range with fp16's
+  // precision): there the queries are carried in fp16 (see the q load)
+  using MT = typename std::conditional<F8, __half, T>::type;
   static_assert(NSUB == 1 || NSUB == 2, "one or two sub-tiles per step");
   static_assert(S * NSUB <= 16, "stage bits");
   constexpr int kStepBytes = 2 * NSUB * Sh::kTileBytes;  // K and V of one step
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(NW * 32)
   // chunks q_chunk(i, c); FP8 caches use 16-dim units 2c + j (two chunks each)
   const int G = a.group;
   uint4 qf[Sh::kQChunks];
+  float scale_log2 = a.scale_log2;
   {
     const T *qrow = static_cast<const T *>(a.query) +
                     (static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + g) * D;
@@ -295,6 +301,37 @@ __global__ void __launch_bounds__(NW * 32)
     for (int i = 0; i < Sh::kQChunks; ++i) {
       const int ch = F8 ? 2 * (2 * c + (i >> 1)) + (i & 1) : q_chunk(i, c);
       qf[i] = g < G ? *reinterpret_cast<const uint4 *>(qrow + ch * 8) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (F8 && !std::is_same<T, __half>::value) {
+      // bf16 queries over FP8 caches: the warp holds all G x D query values;
+      // scale them by 2^e so the largest magnitude lands in [2^14, 2^15),
+      // then round to fp16 (exact for every value down to 2^-31 of the
+      // largest: bf16 carries 8 significant bits, and fp16 holds 8 bits at
+      // every magnitude from 2^-17 up), and fold 2^-e into the softmax scale
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < Sh::kQChunks; ++i)
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+          const float2 v = Elem<T>::unpack(word_of(qf[i], w2));
+          mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+        }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+      const int e = min(120, 14 - ex);
+      const float f = ldexpf(1.f, e);
+#pragma unroll
+      for (int i = 0; i < Sh::kQChunks; ++i) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+          const float2 v = Elem<T>::unpack(word_of(qf[i], w2));
+          w4[w2] = Elem<__half>::pack(v.x * f, v.y * f);
+        }
+        qf[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      scale_log2 = ldexpf(scale_log2, -e);
     }
   }
 
@@ -339,8 +376,8 @@ __global__ void __launch_bounds__(NW * 32)
           const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
           const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
           const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
-          Elem<T>::mma(sc[h], ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
-          Elem<T>::mma(sc[h], ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
+          Elem<MT>::mma(sc[h], ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
+          Elem<MT>::mma(sc[h], ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
         }
       } else {
         // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
@@ -355,7 +392,7 @@ __global__ void __launch_bounds__(NW * 32)
                                  qf[2 * j + 1].w};
 #pragma unroll
           for (int t = 0; t < 4; ++t)
-            Elem<T>::mma(sc[h], ka[2 * t], kb[2 * t], ka[2 * t + 1], kb[2 * t + 1], q[2 * t],
+            Elem<MT>::mma(sc[h], ka[2 * t], kb[2 * t], ka[2 * t + 1], kb[2 * t + 1], q[2 * t],
                          q[2 * t + 1]);
         }
       }
@@ -368,10 +405,10 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int h = 0; h < NSUB; ++h) {
       const bool v_lo = g < nvalid[h], v_hi = g + 8 < nvalid[h];
-      x[h][0] = v_lo ? sc[h][0] * a.scale_log2 : NEG_INF;
-      x[h][1] = v_lo ? sc[h][1] * a.scale_log2 : NEG_INF;
-      x[h][2] = v_hi ? sc[h][2] * a.scale_log2 : NEG_INF;
-      x[h][3] = v_hi ? sc[h][3] * a.scale_log2 : NEG_INF;
+      x[h][0] = v_lo ? sc[h][0] * scale_log2 : NEG_INF;
+      x[h][1] = v_lo ? sc[h][1] * scale_log2 : NEG_INF;
+      x[h][2] = v_hi ? sc[h][2] * scale_log2 : NEG_INF;
+      x[h][3] = v_hi ? sc[h][3] * scale_log2 : NEG_INF;
       mx0 = fmaxf(mx0, fmaxf(x[h][0], x[h][2]));
       mx1 = fmaxf(mx1, fmaxf(x[h][1], x[h][3]));
     }
@@ -415,13 +452,13 @@ __global__ void __launch_bounds__(NW * 32)
       // carried as hi + lo in the MMA type (hi = P rounded, lo = the exact fp32
       // remainder rounded), so the P.V product keeps ~16 (bf16) or ~22 (fp16)
       // bits of P instead of 8 or 11.
-      const uint32_t h01 = Elem<T>::pack(p[h][0], p[h][1]);
-      const uint32_t h23 = Elem<T>::pack(p[h][2], p[h][3]);
-      const float2 f01 = Elem<T>::unpack(h01), f23 = Elem<T>::unpack(h23);
+      const uint32_t h01 = Elem<MT>::pack(p[h][0], p[h][1]);
+      const uint32_t h23 = Elem<MT>::pack(p[h][2], p[h][3]);
+      const float2 f01 = Elem<MT>::unpack(h01), f23 = Elem<MT>::unpack(h23);
       const uint32_t pb0 = movmatrix_trans(h01);
       const uint32_t pb1 = movmatrix_trans(h23);
-      const uint32_t pr0 = movmatrix_trans(Elem<T>::pack(p[h][0] - f01.x, p[h][1] - f01.y));
-      const uint32_t pr1 = movmatrix_trans(Elem<T>::pack(p[h][2] - f23.x, p[h][3] - f23.y));
+      const uint32_t pr0 = movmatrix_trans(Elem<MT>::pack(p[h][0] - f01.x, p[h][1] - f01.y));
+      const uint32_t pr1 = movmatrix_trans(Elem<MT>::pack(p[h][2] - f23.x, p[h][3] - f23.y));
       const uint8_t *Vs = stage + (NSUB + h) * Sh::kTileBytes;
 
       // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; unit g of every box
@@ -449,8 +486,8 @@ __global__ void __launch_bounds__(NW * 32)
           const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
           const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
           const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
-          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-          Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+          Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+          Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
         }
       } else {
         // unit g (dims 16g .. 16g+15) of each row, still E4M3
@@ -472,14 +509,14 @@ __global__ void __launch_bounds__(NW * 32)
           {
             const uint32_t a0 = e4m3x2_lo_to_f16x2(w0), a1 = e4m3x2_lo_to_f16x2(w1);
             const uint32_t a2 = e4m3x2_lo_to_f16x2(w2), a3 = e4m3x2_lo_to_f16x2(w3);
-            Elem<T>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-            Elem<T>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
+            Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
           }
           {
             const uint32_t a0 = e4m3x2_hi_to_f16x2(w0), a1 = e4m3x2_hi_to_f16x2(w1);
             const uint32_t a2 = e4m3x2_hi_to_f16x2(w2), a3 = e4m3x2_hi_to_f16x2(w3);
-            Elem<T>::mma(acc[mt + 1], a0, a1, a2, a3, pb0, pb1);
-            Elem<T>::mma(acc[mt + 1], a0, a1, a2, a3, pr0, pr1);
+            Elem<MT>::mma(acc[mt + 1], a0, a1, a2, a3, pb0, pb1);
+            Elem<MT>::mma(acc[mt + 1], a0, a1, a2, a3, pr0, pr1);
           }
         }
       }
@@ -821,7 +858,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
     return cudaErrorInvalidValue;
   }
   if (kv_fp8)
-    return launch_decode_t<__half, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream);
+    return dtype == 0
+               ? launch_decode_t<__half, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream)
+               : launch_decode_t<__nv_bfloat16, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
+                                                                                       stream);
   if (dtype == 0) {
     return head_dim == 128
                ? launch_decode_t<__half, 128, kWarps, kStages, false, kNsub>(a, km, vm, stream)

@@ -44,15 +44,15 @@ def run_fp8(pa, w, partition_sizes):
     return kc, vc, outs
 
 
-def host_pool(w, src_dtype="fp16"):
+def host_pool(w):
     kh, vh = w.k_cache.numpy().copy(), w.v_cache.numpy().copy()
-    oracle.reshape_and_cache_fp8(w.key, w.value, kh, vh, w.slot_mapping, src_dtype, w.k_scale,
+    oracle.reshape_and_cache_fp8(w.key, w.value, kh, vh, w.slot_mapping, w.dtype, w.k_scale,
                                  w.v_scale)
     return kh, vh
 
 
 def check(w, kh, vh, outs, pairs=None):
-    ref = oracle.decode(w.query, kh, vh, w.block_tables, w.context_lens, w.scale, "fp16",
+    ref = oracle.decode(w.query, kh, vh, w.block_tables, w.context_lens, w.scale, w.dtype,
                         pairs=pairs, kv_dtype="e4m3", k_scale=w.k_scale, v_scale=w.v_scale)
     for ps, out in outs.items():
         got = out.float().cpu().double().numpy()
@@ -68,7 +68,12 @@ def check(w, kh, vh, outs, pairs=None):
 CASES = [("llama3_8b_gqa", dict(lens=[1, 15, 16, 17, 100, 513, 2049], num_q_heads=32)),
          ("llama3_70b_cb", dict(lens=[1, 31, 32, 33, 700, 3000])),
          ("llama3_8b_gqa", dict(lens=[40, 300], num_q_heads=8, num_kv_heads=8)),     # G = 1
-         ("long_context", dict(lens=[9000, 3], dtype="fp16"))]
+         ("long_context", dict(lens=[9000, 3], dtype="fp16")),
+         # bf16 queries (carried in fp16 under a power-of-two rescale)
+         ("llama3_70b_cb", dict(lens=[1, 31, 32, 33, 700, 3000], dtype="bf16")),
+         ("long_context", dict(lens=[9000, 3])),
+         ("llama3_8b_gqa", dict(lens=[5, 600], num_q_heads=24, num_kv_heads=8, block_size=32,
+                                dtype="bf16"))]
 
 
 @pytest.mark.parametrize("name,kw", CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(CASES)])
@@ -80,14 +85,16 @@ def test_fp8_small_cases(pa, name, kw):
     check(w, kh, vh, outs)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_gqa", "llama3_70b_cb"])
-def test_fp8_full_size(pa, name):
-    w = W.to_fp8(W.make(name, 0))
+@pytest.mark.parametrize("name,dtype", [("llama3_8b_gqa", "fp16"), ("llama3_70b_cb", "fp16"),
+                                        ("llama3_70b_cb", "bf16"), ("long_context", "bf16")])
+def test_fp8_full_size(pa, name, dtype):
+    w = W.to_fp8(W.make(name, 0, dtype=dtype))
     kc, vc, outs = run_fp8(pa, w, [w.partition_size])
     kh, vh = host_pool(w)
     assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
     rng = np.random.default_rng(0)
-    seqs = sorted(set(rng.choice(w.num_seqs, 16, replace=False).tolist()) |
+    n = 2 if name == "long_context" else 16   # the long sequences are slow in the oracle
+    seqs = sorted(set(rng.choice(w.num_seqs, n, replace=False).tolist()) |
                   {int(w.context_lens.argmax())})
     check(w, kh, vh, outs, pairs=[(i, h) for i in seqs for h in range(w.num_q_heads)])
 
@@ -100,11 +107,27 @@ def test_fp8_random_shapes(pa, i):
     G, hkv = int(rng.integers(1, 9)), int(rng.choice([1, 2, 4, 8]))
     lens = [int(x) for x in rng.integers(0, 3001, int(rng.integers(1, 9)))]
     w = W.to_fp8(W.make("llama3_8b_gqa", 120 + i, lens=lens, num_q_heads=G * hkv,
-                        num_kv_heads=hkv, block_size=int(rng.choice([16, 32]))))
+                        num_kv_heads=hkv, block_size=int(rng.choice([16, 32])),
+                        dtype=str(rng.choice(["fp16", "bf16"]))))
     ps = int(rng.choice([0, 16, 48, 160, 512]))
     kc, vc, outs = run_fp8(pa, w, [ps])
     kh, vh = host_pool(w)
     assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
+    check(w, kh, vh, outs)
+
+
+@pytest.mark.parametrize("scales", [(3e4, 3e4), (1e-6, 1e-6), (1e3, 1e-7), (1.0, 0.0)],
+                         ids=["large", "tiny", "mixed", "one-head-zero"])
+def test_fp8_bf16_query_magnitudes(pa, scales):
+    """bf16 queries far from 1, and heads of very different magnitude in one
+    query group (the power-of-two rescale is per sequence and KV head)."""
+    w = W.to_fp8(W.make("llama3_8b_gqa", 46, lens=[300, 1000, 17], dtype="bf16"))
+    q = w.query.float()
+    q[:, 0::4] *= scales[0]
+    q[:, 1::4] *= scales[1]
+    w.query = q.to(torch.bfloat16)
+    kc, vc, outs = run_fp8(pa, w, [0, 512])
+    kh, vh = host_pool(w)
     check(w, kh, vh, outs)
 
 
