@@ -233,7 +233,8 @@ def cpu_oracle_run(w, budget_s: float, threads: int = 0):
     """Time the oracle (scatter + fp64 decode) on a bounded sample: the first
     n sequences, n grown until one run takes a good part of the budget; when
     the whole batch is quicker than that, the run is repeated until about two
-    thirds of the budget is spent.  ``threads`` = 0 uses every host core.
+    thirds of the budget is spent.  ``threads`` = 0 uses every core this
+    process may run on.
     Returns (GB/s, threads used, sample description, seconds, n)."""
     import numpy as np
     import torch
@@ -245,7 +246,9 @@ def cpu_oracle_run(w, budget_s: float, threads: int = 0):
     else:
         kh = w.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
         vh = w.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
-    cores = threads if threads > 0 else oracle.max_threads()
+    # an explicit count every time: the oracle's OpenMP thread count persists
+    # from one call to the next
+    cores = threads if threads > 0 else len(os.sched_getaffinity(0))
 
     def one_run(n):
         sub = slice(0, n)
@@ -256,7 +259,7 @@ def cpu_oracle_run(w, budget_s: float, threads: int = 0):
         else:
             oracle.reshape_and_cache(w.key[sub], w.value[sub], kh, vh, w.slot_mapping[sub])
         oracle.decode(w.query[sub], kh, vh, w.block_tables[sub], w.context_lens[sub], w.scale,
-                      w.dtype, partition_size=w.partition_size, threads=threads,
+                      w.dtype, partition_size=w.partition_size, threads=cores,
                       kv_dtype="e4m3" if fp8 else None, k_scale=w.k_scale, v_scale=w.v_scale)
         return time.perf_counter() - t0
 
