@@ -263,13 +263,18 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       }
       tc_fence_after();
       float sv[kPairKeys];
-#pragma unroll
-      for (int q = 0; q < kPairKeys / 32; ++q) {
-        float t0[32];
-        tmem_ld32(lane_addr + 32 * q, t0);
+      static_assert(kPairKeys == 64, "two 32-column loads");
+      {
+        // both loads in flight before the one wait
+        float t0[32], t1[32];
+        tmem_ld32(lane_addr, t0);
+        tmem_ld32(lane_addr + 32, t1);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 * q + i] = t0[i];
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = t0[i];
+          sv[32 + i] = t1[i];
+        }
       }
       // the score columns may now take the next step's Q K^T
       tc_fence_before();
@@ -424,19 +429,27 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
         const uint32_t qb = smem_addr(smem + L::kQOff) + t * kAtoms * kPairQAtom;
         const uint32_t sk0 = smem_addr(smem + L::kKOff);
+        // descriptors of the tile's Q and of K stage 0; every other operand
+        // is these plus a byte offset / 16 in the address field (shared
+        // memory lies below 2^18 bytes, so the 14-bit field never carries)
+        const uint64_t dq0 = umma_desc_sw128(qb, 16, 1024);
+        const uint64_t dk0 = umma_desc_sw128(sk0, 16, 1024);
         ok_run = mbar_wait_bounded(q_ready, 0);
         for (int n = 0; n < nt && ok_run; ++n) {
-          if ((n > 0 && !mbar_wait_bounded(&s_free[t], (n - 1) & 1)) ||
-              !mbar_wait_bounded(&k_full[n % SK], (n / SK) & 1)) {
+          // K is staged well ahead, so wait for it first: then only the
+          // release of the score columns stands between the softmax and the
+          // next product (that hand-off sets the step time)
+          if (!mbar_wait_bounded(&k_full[n % SK], (n / SK) & 1) ||
+              (n > 0 && !mbar_wait_bounded(&s_free[t], (n - 1) & 1))) {
             ok_run = false;
             break;
           }
           tc_fence_after();
-          const uint32_t kb = sk0 + (n % SK) * kAtoms * kPairKvAtom;
+          const uint64_t dkn = dk0 + static_cast<uint64_t>(((n % SK) * kAtoms * kPairKvAtom) >> 4);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint64_t da = umma_desc_sw128(qb + (k >> 2) * kPairQAtom + (k & 3) * 32, 16, 1024);
-            const uint64_t db = umma_desc_sw128(kb + (k >> 2) * kPairKvAtom + (k & 3) * 32, 16, 1024);
+            const uint64_t da = dq0 + static_cast<uint64_t>(((k >> 2) * kPairQAtom + (k & 3) * 32) >> 4);
+            const uint64_t db = dkn + static_cast<uint64_t>(((k >> 2) * kPairKvAtom + (k & 3) * 32) >> 4);
             umma_f16(tt, da, db, id_qk, k > 0);
           }
           umma_commit(&s_full[t]);
@@ -452,6 +465,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       } else {
         const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, D);
         const uint32_t sv0 = smem_addr(smem + L::kVOff);
+        const uint64_t dv0 = umma_desc_sw128(sv0, kPairKvAtom, 1024);  // V stage 0, as for K
         for (int n = 0; n < nt && ok_run; ++n) {
           const int s = n % SV, pb = n % kPBufs;
           if (!mbar_wait_bounded(&p_full[2 * t + pb], (n / kPBufs) & 1) ||
@@ -460,10 +474,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
             break;
           }
           tc_fence_after();
-          const uint32_t vb = sv0 + s * kAtoms * kPairKvAtom;
+          const uint64_t dvs = dv0 + static_cast<uint64_t>((s * kAtoms * kPairKvAtom) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kPairKeys / 16; ++kk) {
-            const uint64_t dv = umma_desc_sw128(vb + kk * 2048, kPairKvAtom, 1024);
+            const uint64_t dv = dvs + static_cast<uint64_t>((kk * 2048) >> 4);
             if constexpr (SPLIT) {
               umma_f16_ts(tt + kOCol, tt + kPCol + 8 * kk, dv, id_pv, n > 0 || kk > 0);
               umma_f16_ts(tt + kOCol, tt + kPCol + 32 + 8 * kk, dv, id_pv, true);
