@@ -205,8 +205,8 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
  * max_q_len      >= every q_len_i (sizes the launch)
  * Softmax and accumulation fp32; out rounded to dtype.  scale > 0.  head_dim
  * in {64, 128}, block_size in {16, 32}, num_q_heads / num_kv_heads in 1..8
- * (head_dim 128 with a group G of 1, 2, 4 or 8 runs on tcgen05 kernels: two
- * 128-row query tiles per CTA when max_q_len * G > 128, one otherwise).  A
+ * (every shape runs on the tcgen05 kernel: two 128-row query tiles per CTA
+ * when max_q_len * G > 128, one otherwise).  A
  * q_len_i larger than context_lens[i] or than max_q_len, or a context longer
  * than the table, skips that sequence and sets PA_DEVERR_BAD_LEN.  A block id
  * outside [0, num_blocks) for a token in use sets PA_DEVERR_BAD_BLOCK; that
