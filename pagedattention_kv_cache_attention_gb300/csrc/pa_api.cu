@@ -157,7 +157,9 @@ pa_status reduce_impl(void *out, const void *workspace, const int32_t *context_l
   if (num_seqs == 0) return PA_OK;
   if (!out || !workspace || !context_lens || !aligned16(out) || !aligned16(workspace))
     return PA_ERR_INVALID_ARG;
-  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  // one CTA per output row
+  if (num_seqs > 65535 || static_cast<int64_t>(num_seqs) * num_q_heads > 0x7fffffff)
+    return PA_ERR_UNSUPPORTED;
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
   const int32_t P = num_partitions(max_context_len, partition_size);
@@ -175,6 +177,9 @@ pa_status reduce_impl(void *out, const void *workspace, const int32_t *context_l
   a.partition_size = partition_size;
   a.max_context_len = max_context_len;
   a.table_tokens = table_tokens;
+  // more warps per row when rows hold many partitions (measured: one warp per
+  // row up to 64 partitions; four for the 256 of a 131k-token context)
+  a.warps_per_row = P > 128 ? 4 : (P > 64 ? 2 : 1);
   a.err = err;
   return pa::launch_reduce(a, head_dim, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK

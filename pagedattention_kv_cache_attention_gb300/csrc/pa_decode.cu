@@ -163,7 +163,14 @@ __device__ __forceinline__ void join_partitions(const DecodeArgs &a, int seq, in
 // (T is then fp16), converted exactly to fp16 in registers.  NSUB: 16-token
 // sub-tiles per pipeline step (their MMA chains are independent and share one
 // softmax reduction).
-template <typename T, int D, int NW, int S, bool F8, int NSUB>
+// WP ("warp partitions"): each warp takes a whole partition (CTA x serves
+// partitions x NW .. x NW + NW - 1 of its sequence and KV head) and writes that
+// partition's partial from its own registers, with no merge across warps; used
+// when the partitions are joined by the reduce kernel (more of them than the
+// in-kernel join takes), so a CTA pays one pipeline ramp and one epilogue for
+// NW partitions -- short partitions gain the most.  Otherwise the NW warps
+// share one partition.
+template <typename T, int D, int NW, int S, bool F8, int NSUB, bool WP>
 __global__ void __launch_bounds__(NW * 32)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
@@ -182,8 +189,9 @@ __global__ void __launch_bounds__(NW * 32)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * kStepBytes);
 
-  const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int kvh = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = WP ? blockIdx.x * NW + warp : blockIdx.x;
   const int g = lane >> 2, c = lane & 3;
 
   uint8_t *my_stages = smem + warp * S * kStepBytes;
@@ -199,16 +207,19 @@ __global__ void __launch_bounds__(NW * 32)
   grid_dependency_wait();
 
   // Step k of warp w covers sub-tiles (w + k NW) NSUB + h, h < NSUB, of the
-  // partition.  A "local" sub-tile index l = k NSUB + h numbers the warp's
-  // sub-tiles in order; lane l of a window holds the block id of local
-  // sub-tile (window base + l).  The first window is read before the context
+  // partition (WP: sub-tiles k NSUB + h of the warp's own partition).  A
+  // "local" sub-tile index l = k NSUB + h numbers the warp's sub-tiles in
+  // order; lane l of a window holds the block id of local sub-tile (window
+  // base + l).  The first window is read before the context
   // length arrives (entries past the sequence are read from the table row but
   // never used).
   const int t_begin = part * a.part_tokens;
   const int full_sub = (a.part_tokens + kTile - 1) / kTile;
   const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
   const int bs_mask = (1 << a.bs_log2) - 1;
-  auto sub_of = [&](int l) { return (warp + (l / NSUB) * NW) * NSUB + (l % NSUB); };
+  auto sub_of = [&](int l) {
+    return WP ? l : (warp + (l / NSUB) * NW) * NSUB + (l % NSUB);
+  };
   auto table_entry = [&](int l) -> int {
     const int u = sub_of(l);
     if (u >= full_sub) return -1;
@@ -229,7 +240,8 @@ __global__ void __launch_bounds__(NW * 32)
   const int t_end = min(ctx, t_begin + a.part_tokens);
   const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int n_grp = (n_sub + NSUB - 1) / NSUB;
-  const int my_n = n_grp > warp ? (n_grp - warp + NW - 1) / NW : 0;  // this warp's steps
+  // this warp's steps
+  const int my_n = WP ? n_grp : (n_grp > warp ? (n_grp - warp + NW - 1) / NW : 0);
 
   // physical block of local sub-tile l, -1 if past the partition or invalid
   // (an invalid entry is flagged and its tokens are masked)
@@ -558,6 +570,43 @@ __global__ void __launch_bounds__(NW * 32)
     l1 += __shfl_xor_sync(kFull, l1, off);
   }
 
+  if constexpr (WP) {
+    // the warp's partition is complete: write its (m, l, o) for heads 2c and
+    // 2c + 1 straight from the fragments (o normalised, times the V scale)
+    const int64_t row0 = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G;
+    const int h0 = 2 * c, h1 = 2 * c + 1;
+    const float inv0 = l0 > 0.f ? a.out_scale / l0 : 0.f;
+    const float inv1 = l1 > 0.f ? a.out_scale / l1 : 0.f;
+    const int64_t pr0 = (row0 + h0) * a.num_parts + part, pr1 = (row0 + h1) * a.num_parts + part;
+    if (g == 0) {
+      if (h0 < G) {
+        a.ws_m[pr0] = m0;
+        a.ws_l[pr0] = l0;
+      }
+      if (h1 < G) {
+        a.ws_m[pr1] = m1;
+        a.ws_l[pr1] = l1;
+      }
+    }
+    float *o0 = a.ws_o + pr0 * D;
+    float *o1 = a.ws_o + pr1 * D;
+#pragma unroll
+    for (int mt = 0; mt < Sh::kMTiles; ++mt) {
+      const int dA = F8 ? 16 * g + mt : 8 * g + mt;
+      const int dB = F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
+      if (h0 < G) {
+        o0[dA] = acc[mt][0] * inv0;
+        o0[dB] = acc[mt][2] * inv0;
+      }
+      if (h1 < G) {
+        o1[dA] = acc[mt][1] * inv1;
+        o1[dB] = acc[mt][3] * inv1;
+      }
+    }
+    grid_launch_dependents();
+    return;
+  }
+
   // ---- merge warps through shared memory (stages are idle now)
   __syncthreads();
   float *wacc = reinterpret_cast<float *>(smem);  // [NW][8][D]
@@ -645,112 +694,127 @@ __global__ void __launch_bounds__(NW * 32)
   grid_launch_dependents();
 }
 
-// Log-sum-exp join of partitions: one warp per output row (sequence, query
-// head), four rows per CTA.  Lanes read the partitions' (m, l) 32 at a time and
-// turn them into weights l_p 2^(m_p - M); every lane then accumulates its
-// head_dim / 32 output elements over the partitions' o rows.
-constexpr int kReduceRows = 4;
+// Log-sum-exp join of partitions when a call has more of them than the decode
+// kernel joins itself (and behind the exported pa_decode_reduce).  A CTA of
+// four warps serves 4 / WPR output rows (sequence, query head), WPR warps per
+// row: warp j of a row takes partitions j, j + WPR, ... with a running
+// maximum, eight partitions per round trip to memory (each lane holds
+// head_dim / 32 output elements of every partition it reads), and the row's
+// warps combine their (M, L, acc) through shared memory.  The host picks WPR
+// from the partition count: one warp per row when rows hold few partitions
+// (fewer, fuller CTAs), four when they hold many (a row of 256 partitions then
+// costs eight round trips per warp).
+constexpr int kReduceWarps = 4;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kReduceRows * 32) pa_decode_reduce_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kReduceWarps * 32) pa_decode_reduce_kernel(const ReduceArgs a) {
   constexpr int kPer = D / 32;  // output elements per lane
+  constexpr int kGroup = 8;     // partitions in flight per warp
+  __shared__ float s_m[kReduceWarps], s_l[kReduceWarps];
+  __shared__ __align__(16) float s_acc[kReduceWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kReduceRows + warp;
+  const int wpr = a.warps_per_row;               // 1, 2 or 4
+  const int j = warp % wpr;                      // this warp's place in its row
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kReduceWarps / wpr) + warp / wpr;
   grid_dependency_wait();  // the partials come from the decode grid
-  if (row >= static_cast<int64_t>(a.num_seqs) * a.num_q_heads) return;
-  const int seq = static_cast<int>(row / a.num_q_heads);
-  int ctx = a.context_lens[seq];
-  // the same validity test as the decode kernel, so a length it refused joins
-  // no partitions (none of them were written by this call)
-  if (ctx < 0 || ctx > a.max_context_len || ctx > a.table_tokens) {
-    if (lane == 0 && row % a.num_q_heads == 0) atomicOr(a.err, kErrBadLen);
-    ctx = 0;
-  }
-  const int np = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 0;
-  const float *m = a.ws_m + row * a.num_parts;
-  const float *l = a.ws_l + row * a.num_parts;
-  const float *o = a.ws_o + row * a.num_parts * D + lane * kPer;
-
-  // the partials of up to kPre partitions are loaded together with (m, l), so
-  // the common case (a handful of partitions) takes one round trip after the
-  // context length instead of two
-  constexpr int kPre = 8;
-  float xo[kPre][kPer];
-#pragma unroll
-  for (int u = 0; u < kPre; ++u) {
-    if (u < np) {
-      if constexpr (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(o + static_cast<int64_t>(u) * D);
-        xo[u][0] = v.x;
-        xo[u][1] = v.y;
-        xo[u][2] = v.z;
-        xo[u][3] = v.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) xo[u][e] = o[static_cast<int64_t>(u) * D + e];
-      }
+  const bool row_ok = row < static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  int np = 0;
+  if (row_ok) {
+    const int seq = static_cast<int>(row / a.num_q_heads);
+    int ctx = a.context_lens[seq];
+    // the same validity test as the decode kernel, so a length it refused
+    // joins no partitions (none of them were written by this call)
+    if (ctx < 0 || ctx > a.max_context_len || ctx > a.table_tokens) {
+      if (lane == 0 && j == 0 && row % a.num_q_heads == 0) atomicOr(a.err, kErrBadLen);
+      ctx = 0;
     }
+    np = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 0;
   }
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) M = fmaxf(M, m[p]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  const int64_t rr = row_ok ? row : 0;
+  const float *m = a.ws_m + rr * a.num_parts;
+  const float *l = a.ws_l + rr * a.num_parts;
+  const float *o = a.ws_o + rr * a.num_parts * D + lane * kPer;
 
-  float acc[kPer];
+  float M = -INFINITY, L = 0.f, acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  for (int p0 = 0; p0 < np; p0 += 32) {
-    const int p = p0 + lane;
-    float wgt = 0.f;
-    if (p < np) {
-      const float mp = m[p];
-      wgt = mp == -INFINITY ? 0.f : l[p] * exp2f(mp - M);
-    }
-    L += wgt;
-    const int cnt = min(32, np - p0);
-    int j = 0;
-    if (p0 == 0) {
+  for (int p0 = j; p0 < np; p0 += wpr * kGroup) {
+    float mp[kGroup], lp[kGroup], op[kGroup][kPer];
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        if (u < cnt) {
-          const float wj = __shfl_sync(kFull, wgt, u);
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) acc[e] += wj * xo[u][e];
+    for (int u = 0; u < kGroup; ++u) {
+      const int p = p0 + u * wpr;
+      if (p < np) {
+        mp[u] = m[p];
+        lp[u] = l[p];
+        const float *src = o + static_cast<int64_t>(p) * D;
+        if constexpr (kPer == 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(src);
+          op[u][0] = v.x;
+          op[u][1] = v.y;
+          op[u][2] = v.z;
+          op[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2 *>(src);
+          op[u][0] = v.x;
+          op[u][1] = v.y;
         }
-      }
-      j = min(cnt, kPre);
-    }
-    for (; j + 4 <= cnt; j += 4) {
-      float x[4][kPer];
+      } else {
+        mp[u] = -INFINITY;
+        lp[u] = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) x[u][e] = o[static_cast<int64_t>(p0 + j + u) * D + e];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float wj = __shfl_sync(kFull, wgt, j + u);
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] += wj * x[u][e];
+        for (int e = 0; e < kPer; ++e) op[u][e] = 0.f;
       }
     }
-    for (; j < cnt; ++j) {
-      const float wj = __shfl_sync(kFull, wgt, j);
+    float Mn = M;
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] += wj * o[static_cast<int64_t>(p0 + j) * D + e];
+    for (int u = 0; u < kGroup; ++u) Mn = fmaxf(Mn, mp[u]);
+    const float ref = Mn == -INFINITY ? 0.f : Mn;  // no token yet: any finite reference
+    const float al = exp2f(M - ref);
+    L *= al;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] *= al;
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const float wgt = lp[u] * exp2f(mp[u] - ref);
+      L += wgt;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] += wgt * op[u][e];
     }
+    M = Mn;
+  }
+
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_l[warp] = L;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint32_t packed[kPer / 2];
+  for (int e = 0; e < kPer; ++e) s_acc[warp][lane * kPer + e] = acc[e];
+  __syncthreads();
+  if (j == 0 && row_ok) {
+    // the row's warps are warp .. warp + wpr - 1
+    float Mt = -INFINITY;
+    for (int w = warp; w < warp + wpr; ++w) Mt = fmaxf(Mt, s_m[w]);
+    const float ref = Mt == -INFINITY ? 0.f : Mt;
+    float Lt = 0.f, out[kPer];
 #pragma unroll
-  for (int e = 0; e < kPer / 2; ++e) packed[e] = Elem<T>::pack(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-  T *dst = static_cast<T *>(a.out) + row * D + lane * kPer;
-  if constexpr (kPer == 4) {
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-  } else {
-    *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    for (int e = 0; e < kPer; ++e) out[e] = 0.f;
+    for (int w = warp; w < warp + wpr; ++w) {
+      const float f = exp2f(s_m[w] - ref);
+      Lt += s_l[w] * f;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) out[e] += s_acc[w][lane * kPer + e] * f;
+    }
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    uint32_t packed[kPer / 2];
+#pragma unroll
+    for (int e = 0; e < kPer / 2; ++e)
+      packed[e] = Elem<T>::pack(out[2 * e] * inv, out[2 * e + 1] * inv);
+    T *dst = static_cast<T *>(a.out) + row * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+      *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    }
   }
 }
 
@@ -794,8 +858,8 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_
 
 namespace {
 
-template <typename T, int D, int NW, int S, bool F8, int NSUB>
-cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+template <typename T, int D, int NW, int S, bool F8, int NSUB, bool WP>
+cudaError_t launch_decode_w(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
                             cudaStream_t stream) {
   using Sh = Shape<D, F8>;
   constexpr size_t step = 2 * NSUB * Sh::kTileBytes;
@@ -803,20 +867,33 @@ cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CU
   static_assert(static_cast<size_t>(NW) * 8 * D * 4 + NW * 8 * 2 * 4 + 16 <=
                     static_cast<size_t>(NW) * S * step,
                 "merge buffers and the join flag must fit in the stage area");
-  auto kern = pa_decode_kernel<T, D, NW, S, F8, NSUB>;
+  auto kern = pa_decode_kernel<T, D, NW, S, F8, NSUB, WP>;
   static SmemLimitOnce smem_limit;
   const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3(a.num_parts, a.num_kv_heads, a.num_seqs), dim3(NW * 32),
-                          smem, stream, km, vm, a);
+  const unsigned gx = WP ? static_cast<unsigned>((a.num_parts + NW - 1) / NW)
+                         : static_cast<unsigned>(a.num_parts);
+  return launch_dependent(kern, dim3(gx, a.num_kv_heads, a.num_seqs), dim3(NW * 32), smem, stream,
+                          km, vm, a);
+}
+
+// Warp partitions when the partitions are joined by the reduce kernel; one
+// partition per CTA otherwise (including the in-kernel join).
+template <typename T, int D, int NW, int S, bool F8, int NSUB>
+cudaError_t launch_decode_t(const DecodeArgs &a, const CUtensorMap &km, const CUtensorMap &vm,
+                            cudaStream_t stream) {
+  return a.num_parts > 1 && !a.fuse_join
+             ? launch_decode_w<T, D, NW, S, F8, NSUB, true>(a, km, vm, stream)
+             : launch_decode_w<T, D, NW, S, F8, NSUB, false>(a, km, vm, stream);
 }
 
 template <typename T, int D>
 cudaError_t launch_reduce_t(const ReduceArgs &a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const int rows_per_cta = kReduceWarps / a.warps_per_row;
   return launch_dependent(pa_decode_reduce_kernel<T, D>,
-                          dim3(static_cast<unsigned>((rows + kReduceRows - 1) / kReduceRows)),
-                          dim3(kReduceRows * 32), 0, stream, a);
+                          dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta)),
+                          dim3(kReduceWarps * 32), 0, stream, a);
 }
 
 }  // namespace

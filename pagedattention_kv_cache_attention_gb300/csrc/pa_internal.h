@@ -68,6 +68,7 @@ struct ReduceArgs {
   // longer context is treated as invalid exactly as the decode kernel treats
   // it (INT32_MAX when the partials do not come from pa_decode)
   int64_t table_tokens;
+  int warps_per_row;            // 1, 2 or 4 warps join one row
   unsigned *err;
 };
 
