@@ -698,18 +698,18 @@ __global__ void __launch_bounds__(NW * 32)
 // kernel joins itself (and behind the exported pa_decode_reduce).  A CTA of
 // four warps serves 4 / WPR output rows (sequence, query head), WPR warps per
 // row: warp j of a row takes partitions j, j + WPR, ... with a running
-// maximum, eight partitions per round trip to memory (each lane holds
+// maximum, sixteen partitions per round trip to memory (each lane holds
 // head_dim / 32 output elements of every partition it reads), and the row's
 // warps combine their (M, L, acc) through shared memory.  The host picks WPR
 // from the partition count: one warp per row when rows hold few partitions
 // (fewer, fuller CTAs), four when they hold many (a row of 256 partitions then
-// costs eight round trips per warp).
+// costs four round trips per warp).
 constexpr int kReduceWarps = 4;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) pa_decode_reduce_kernel(const ReduceArgs a) {
   constexpr int kPer = D / 32;  // output elements per lane
-  constexpr int kGroup = 8;     // partitions in flight per warp
+  constexpr int kGroup = 16;    // partitions in flight per warp
   __shared__ float s_m[kReduceWarps], s_l[kReduceWarps];
   __shared__ __align__(16) float s_acc[kReduceWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
