@@ -6,7 +6,7 @@ split-context partitions joined by log-sum-exp when the workload uses them).
 
 Default workload: the Llama-3-70B-shaped continuous-batching decode batch (256
 sequences, 64 query / 8 KV heads, head_dim 128, block_size 32, context lengths
-lognormal with median 1024 clipped to [1, 16384], fp16, 1024-token partitions),
+lognormal with median 1024 clipped to [1, 16384], fp16, 2048-token partitions),
 the largest of the decode batches.  Measured in the same run and reported
 under `extra_workloads`: the Llama-3-8B-shaped GQA batch (64 sequences, 32/8
 heads, block_size 16, context lengths U[512,4096], fp16) and the 70B batch in
@@ -105,16 +105,20 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, partition_size: int):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel source at the same
+    split-context partition size."""
     path = os.path.join(ROOT, "profiles", f"pa_decode_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != decode_source_hash():
+    m_ps = re.search(r"partition_size:\s*([0-9]+)", text)
+    if not m_src or not m_tr or not m_ps or m_src.group(1) != decode_source_hash():
+        return None
+    if int(m_ps.group(1)) != int(partition_size):
         return None
     return int(m_tr.group(1))
 
@@ -475,18 +479,19 @@ def run_ours(args):
     S = Step(pa, w, dev)
     fp8 = S.fp8
 
-    for _ in range(args.warmup):
-        S.step(stream)
-    torch.cuda.synchronize(dev)
-    if pa.pa_device_errors(stream) != 0:
-        raise RuntimeError("device error bits raised during warm-up")
-
     K = args.steps
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    # timed region: K back-to-back steps, events only at its two ends
+    # the clock sampler starts first, so that the warm-up steps run right
+    # before the timed region (no idle gap for the GPU to drop its clocks in)
     with ClockSampler(dev.index) as clk:
+        for _ in range(args.warmup):
+            S.step(stream)
+        torch.cuda.synchronize(dev)
+        if pa.pa_device_errors(stream) != 0:
+            raise RuntimeError("device error bits raised during warm-up")
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        # timed region: K back-to-back steps, events only at its two ends
         step_ms = time_steps(lambda: S.step(stream), K, stream, dev)
     if dist:
         dist.barrier()
@@ -688,10 +693,10 @@ def run_ours(args):
                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
                          # the committed summaries profile the default launch of each
-                         # workload (its own dtype and partition size, 16-bit cache)
-                         "traffic": (profiled_traffic(w.name) if not fp8
-                                     and not shape_overrides(args)
-                                     and args.partition_size is None else None),
+                         # workload (its own dtype and shape, 16-bit cache) and name
+                         # the partition size they were taken at
+                         "traffic": (profiled_traffic(w.name, S.ps) if not fp8
+                                     and not shape_overrides(args) else None),
                          "peak_source": peak_src,
                          "decode_ms": round(decode_ms, 5)},
             "cpu_baseline": cpu,

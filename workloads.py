@@ -22,7 +22,7 @@ Workloads (sizes as the decode batches they stand in for):
   shared_prefix_cow  16 groups x 8 seqs sharing a 2048-token prefix, suffix U[1,512]
   long_context       8 seqs, 32/8 heads, d 128, bs 16, ctx {32768 x6, 65536, 131072}, bf16
   llama3_70b_cb      256 seqs, 64/8 heads, d 128, bs 32, ctx lognormal(ln 1024, 1.0)
-                     clipped to [1,16384], pool +20%, fp16 or bf16, 1024-token partitions
+                     clipped to [1,16384], pool +20%, fp16 or bf16, 2048-token partitions
 """
 from __future__ import annotations
 
@@ -313,7 +313,7 @@ def make(name: str, seed: int = 0, *, dtype: Optional[str] = None, batch: Option
                           1, max_len or 16384).astype(np.int64)
         return _build(name, seed, dtype or "fp16", len(ctx), num_q_heads or 64, num_kv_heads or 8,
                       head_dim or 128, block_size or 32, ctx, 1.2,
-                      partition_size if partition_size is not None else 1024, rng, gen,
+                      partition_size if partition_size is not None else 2048, rng, gen,
                       table_len=max_len or 16384)
     raise KeyError(f"unknown workload {name!r}; known: {NAMES}")
 
