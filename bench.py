@@ -45,8 +45,9 @@ MODEL_LAYERS = {"llama3_8b_gqa": 32, "shared_prefix_cow": 32, "long_context": 32
                 "llama3_70b_cb": 80}
 DEFAULT_WORKLOAD = "llama3_70b_cb"
 # the other decode targets measured beside the default line, in the same run
-DEFAULT_EXTRAS = ("llama3_8b_gqa:fp16", "llama3_70b_cb:bf16")
-DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh")
+DEFAULT_EXTRAS = ("llama3_8b_gqa:fp16", "llama3_70b_cb:bf16", "shared_prefix_cow:shared",
+                  "shared_prefix_cow")
+DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh", "pa_tile.cuh")
 
 
 def algorithmic_bytes(w) -> dict:
@@ -63,8 +64,22 @@ def algorithmic_bytes(w) -> dict:
     T = int((w.slot_mapping.numpy() >= 0).sum())
     # K and V rows: 16-bit values read, cached elements written
     scatter = 2 * T * w.num_kv_heads * w.head_dim * (2 + s) + 8 * w.num_seqs
-    return {"kv": kv, "qo": qo, "tables": tables, "decode": kv + qo + tables,
-            "scatter": scatter, "step": kv + qo + tables + scatter}
+    out = {"kv": kv, "qo": qo, "tables": tables, "decode": kv + qo + tables,
+           "scatter": scatter, "step": kv + qo + tables + scatter}
+    if w.group_start is not None:
+        # K/V rows of distinct physical slots: a row that several sequences
+        # reach through shared blocks counts once (what a decode that reads
+        # each shared block once per group must move)
+        bt = w.block_tables.numpy()
+        used = {}
+        for i, c in enumerate(ctx):
+            for lb in range(int((c + w.block_size - 1) // w.block_size)):
+                b = int(bt[i, lb])
+                used[b] = max(used.get(b, 0), int(min(w.block_size, c - lb * w.block_size)))
+        kv_u = 2 * sum(used.values()) * w.num_kv_heads * w.head_dim * s
+        out.update({"kv_unique": kv_u, "decode_unique": kv_u + qo + tables,
+                    "step_unique": kv_u + qo + tables + scatter})
+    return out
 
 
 def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
@@ -350,12 +365,18 @@ def run_cpu_table(args):
 class Step:
     """One workload resident on the device and the calls of its decode step:
     pa_reshape_and_cache of the new tokens, then pa_decode (or their FP8
-    forms) with a zero-filled workspace allocated once."""
+    forms, or pa_decode_shared_prefix when `shared`) with a zero-filled
+    workspace allocated once."""
 
-    def __init__(self, pa, w, dev):
+    def __init__(self, pa, w, dev, shared=False):
         import torch
         self.pa, self.w, self.dev = pa, w, dev
         self.fp8 = w.kv_dtype == "e4m3"
+        if shared and (w.group_start is None or self.fp8):
+            raise ValueError("the shared-prefix decode needs a 16-bit workload with prefix groups")
+        self.shared = shared
+        if shared:
+            self.gs, self.pl = w.group_start.to(dev), w.prefix_lens.to(dev)
         self.kc, self.vc = w.k_cache.to(dev), w.v_cache.to(dev)
         self.key, self.value = w.key.to(dev), w.value.to(dev)
         self.sm = w.slot_mapping.to(dev)
@@ -383,6 +404,10 @@ class Step:
         if self.fp8:
             pa.pa_decode_fp8(out, qq, self.kc, self.vc, tables, lens, w.scale, w.k_scale,
                              w.v_scale, self.maxctx, self.ps, workspace=self.ws, stream=st)
+        elif self.shared:
+            pa.pa_decode_shared_prefix(out, qq, self.kc, self.vc, tables, lens, self.gs, self.pl,
+                                       w.max_group_size, w.scale, self.maxctx, self.ps,
+                                       workspace=self.ws, stream=st)
         else:
             pa.pa_decode(out, qq, self.kc, self.vc, tables, lens, w.scale, self.maxctx,
                          self.ps, workspace=self.ws, stream=st)
@@ -392,10 +417,12 @@ class Step:
         self.decode(self.q, self.bt, self.cl, st)
 
     def launches_per_step(self) -> int:
-        """Kernels one step launches: the scatter, the decode kernel, and the
-        reduce kernel when the join does not run inside the decode kernel."""
+        """Kernels one step launches: the scatter, the decode kernel, the
+        reduce kernel when the join does not run inside the decode kernel, and
+        the shared-prefix kernel before the decode when sharing applies."""
         fused = self.nparts <= 32 and self.w.num_seqs * self.w.num_kv_heads <= 65536
-        return 2 + (1 if self.nparts > 1 and not fused else 0)
+        return (2 + (1 if self.nparts > 1 and not fused else 0)
+                + (1 if self.shared and self.nparts > 1 else 0))
 
 
 def time_steps(fn, K: int, stream, dev) -> float:
@@ -430,10 +457,12 @@ def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
     import torch
 
     import workloads
-    name, dtype = (spec.split(":") + [None])[:2]
+    name, *flags = spec.split(":")
+    dtype = next((f for f in flags if f in ("fp16", "bf16")), None)
+    shared = "shared" in flags
     w = workloads.make(name, seed=args.seed, **({"dtype": dtype} if dtype else {}))
     ab = algorithmic_bytes(w)
-    s = Step(pa, w, dev)
+    s = Step(pa, w, dev, shared=shared)
     for _ in range(args.warmup):
         s.step(stream)
     torch.cuda.synchronize(dev)
@@ -451,6 +480,14 @@ def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
            "roofline_frac": round(dec_gbs / peak, 4),
            "decode_tokens_per_s": round(w.num_seqs / (ms * 1e-3), 1),
            "gpu_launches_per_step": s.launches_per_step()}
+    if "kv_unique" in ab:
+        # bytes of distinct slots (a shared prefix counted once per group)
+        res["decode"] = "pa_decode_shared_prefix" if shared else "pa_decode"
+        res["unique"] = {"step_gbs": round(ab["step_unique"] / (ms * 1e-3) / 1e9, 2),
+                         "hbm_fraction": round(ab["step_unique"] / (ms * 1e-3) / 1e9 / peak, 4),
+                         "decode_gbs": round(ab["decode_unique"] / (dms * 1e-3) / 1e9, 2),
+                         "roofline_frac": round(ab["decode_unique"] / (dms * 1e-3) / 1e9 / peak,
+                                                4)}
     del s
     torch.cuda.empty_cache()
     return res
@@ -476,7 +513,7 @@ def run_ours(args):
     w = make_workload(args)
     ab = algorithmic_bytes(w)
     stream = torch.cuda.current_stream(dev)
-    S = Step(pa, w, dev)
+    S = Step(pa, w, dev, shared=args.shared_prefix)
     fp8 = S.fp8
 
     K = args.steps
@@ -633,7 +670,9 @@ def run_ours(args):
     e2e_ms = max_over_ranks(pipelined(K), dist, dev)
 
     peak, peak_src = hbm_peak()
-    achieved = ab["decode"] / (decode_ms * 1e-3) / 1e9
+    # the shared-prefix decode must move each shared row once: its roofline
+    # counts distinct slots
+    achieved = ab["decode_unique" if S.shared else "decode"] / (decode_ms * 1e-3) / 1e9
     value_gbs = job_throughput(world, ab["step"], ms_per_step)
     clocks = clk.summary()
 
@@ -685,8 +724,16 @@ def run_ours(args):
             "hbm_fraction": round(value_gbs / world / peak, 4),
             "step_stats": step_stats,
             "bytes_per_step": ab,
+            "unique": None if "kv_unique" not in ab else {
+                "step_gbs": round(job_throughput(world, ab["step_unique"], ms_per_step), 2),
+                "hbm_fraction": round(job_throughput(world, ab["step_unique"], ms_per_step)
+                                      / world / peak, 4),
+                "decode": "pa_decode_shared_prefix" if S.shared else "pa_decode"},
             "roofline": {"bound": "hbm",
-                         "kernel": ("pa_decode call (one decode kernel; the LSE join runs in it)"
+                         "kernel": ("pa_decode_shared_prefix call (shared-prefix kernel + decode "
+                                    "kernel; the LSE join runs in the latter), bytes of distinct "
+                                    "slots" if S.shared else
+                                    "pa_decode call (one decode kernel; the LSE join runs in it)"
                                     if S.launches_per_step() == 2 else
                                     "pa_decode call (decode kernel + LSE reduce kernel)")
                          + ", K event-bracketed calls after the timed steps",
@@ -695,7 +742,7 @@ def run_ours(args):
                          # the committed summaries profile the default launch of each
                          # workload (its own dtype and shape, 16-bit cache) and name
                          # the partition size they were taken at
-                         "traffic": (profiled_traffic(w.name, S.ps) if not fp8
+                         "traffic": (profiled_traffic(w.name, S.ps) if not fp8 and not S.shared
                                      and not shape_overrides(args) else None),
                          "peak_source": peak_src,
                          "decode_ms": round(decode_ms, 5)},
@@ -853,10 +900,12 @@ def main(argv=None):
                     help="step: the decode step (default); blocks: copy/swap block bandwidth; "
                          "prefill: chunked-prefill attention; cpu-table: the oracle on every "
                          "workload at all cores and one core")
-    ap.add_argument("--extra", action="append", default=None, metavar="NAME[:DTYPE]",
+    ap.add_argument("--extra", action="append", default=None, metavar="NAME[:DTYPE][:shared]",
                     help="another workload measured in the same run (repeatable); default: "
                          + ", ".join(DEFAULT_EXTRAS) + " beside the default workload")
     ap.add_argument("--no-extra", action="store_true", help="measure the main workload only")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="decode with pa_decode_shared_prefix (workloads with prefix groups)")
     ap.add_argument("--chunk", type=int, default=512, help="prefill chunk (tokens)")
     ap.add_argument("--head-dim", type=int, default=None, help="override the workload's head_dim")
     ap.add_argument("--q-heads", type=int, default=None, help="override the query head count")
@@ -867,7 +916,8 @@ def main(argv=None):
         args.extra = []
     elif args.extra is None:
         plain = (args.workload == DEFAULT_WORKLOAD and not shape_overrides(args)
-                 and args.partition_size is None and args.kv_dtype == "same")
+                 and args.partition_size is None and args.kv_dtype == "same"
+                 and not args.shared_prefix)
         args.extra = list(DEFAULT_EXTRAS) if plain else []
     if args.impl == "reference":
         return run_reference(args)

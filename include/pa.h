@@ -77,6 +77,10 @@ typedef enum pa_dtype {
 #define PA_DEVERR_TIMEOUT   8u   /* a wait for staged KV data ran past its time limit */
 #define PA_DEVERR_WORKSPACE 16u  /* a split-context join counter in the workspace did not
                                     start at zero (see pa_decode_workspace_size) */
+#define PA_DEVERR_PREFIX    32u  /* pa_decode_shared_prefix: the groups do not cover the batch,
+                                    a group is larger than max_group_size, members of a group
+                                    give different prefix lengths, or a member's table names
+                                    other blocks than the group's for its shared prefix */
 
 /*
  * pa_reshape_and_cache -- write each new token's key and value into its slot
@@ -186,6 +190,51 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
                            int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                            int32_t max_context_len, int32_t partition_size,
                            int32_t dtype, void *stream);
+
+/*
+ * pa_decode_shared_prefix -- pa_decode for a batch whose sequences come in
+ * groups that share a prefix held in the same physical blocks (copy-on-write
+ * sharing: "LLM Serving Engine Shootout", 3.2 Copy-on-Write and 4
+ * RadixAttention; "Serving engines", How vLLM works).  The result is
+ * pa_decode's for the same arguments (the same formula, within rounding);
+ * the difference is the memory traffic: the K/V of a group's shared prefix
+ * is read once per group (per 32 query heads of it) instead of once per
+ * sequence.
+ *
+ * group_start   device int32 [num_groups + 1]: group g is the sequences
+ *               group_start[g] .. group_start[g+1]-1; group_start[0] = 0,
+ *               non-decreasing, group_start[num_groups] = num_seqs (every
+ *               sequence in exactly one group; a sequence that shares nothing
+ *               is a group of its own).
+ * prefix_lens   device int32 [num_seqs]: the number of leading tokens of
+ *               sequence i whose blocks are the same physical blocks for
+ *               every member of its group (equal within a group; 0 = none).
+ *               Only whole partitions of it are shared: member i takes
+ *               partitions p < min(prefix_lens[i] / partition_size,
+ *               ceil(context_lens[i] / partition_size) - 1) from the shared
+ *               pass and the rest from the per-sequence decode.
+ * num_groups    1 .. num_seqs;  max_group_size >= every group's size (sizes
+ *               the launch).
+ * partition_size  > 0, a multiple of 16, at most 8192; with one partition
+ *               (max_context_len <= partition_size) nothing can be shared and
+ *               the call is pa_decode.
+ * Other arguments, the workspace (pa_decode_workspace_size bytes, counter
+ * words zero) and the accuracy are as for pa_decode; dtype fp16 or bf16
+ * caches.  Input errors only the device can see set PA_DEVERR_PREFIX (see
+ * above): the output of the sequences concerned is then unspecified, never a
+ * fault.
+ */
+pa_status pa_decode_shared_prefix(void *out, const void *query,
+                                  const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens,
+                                  const int32_t *group_start, const int32_t *prefix_lens,
+                                  int32_t num_groups, int32_t max_group_size,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                  float scale, int32_t max_context_len, int32_t partition_size,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t dtype, void *stream);
 
 /*
  * pa_prefill -- chunked-prefill attention over the paged cache ("Serving
@@ -372,7 +421,8 @@ pa_status pa_selftest_bounded_wait(void *stream);
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(int32_t status);
 
-/* Library ABI version: 2 (2 added the join counters to the workspace). */
+/* Library ABI version: 3 (2 added the join counters to the workspace, 3
+   pa_decode_shared_prefix). */
 int32_t pa_version(void);
 
 #ifdef __cplusplus

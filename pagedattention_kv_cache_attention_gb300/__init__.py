@@ -26,12 +26,14 @@ __all__ = [
     "pa_decode_static_workspace", "STATIC_WORKSPACE_BYTES", "pa_copy_blocks", "pa_swap_blocks",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill", "pa_selftest_bounded_wait",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
-    "DEVERR_WORKSPACE", "DECODE_COUNTER_BYTES", "new_decode_workspace",
+    "DEVERR_WORKSPACE", "DEVERR_PREFIX", "DECODE_COUNTER_BYTES", "new_decode_workspace",
+    "pa_decode_shared_prefix",
 ]
 
 PA_FP16, PA_BF16 = 0, 1
 DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 DEVERR_WORKSPACE = 16
+DEVERR_PREFIX = 32
 # Bytes of join counters at the start of a split-context workspace
 # (PA_DECODE_COUNTER_BYTES in include/pa.h); they must be zero when a
 # workspace is first used, and every pa_decode call leaves them zero.
@@ -198,6 +200,60 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
         block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, d,
         bs, NB, float(scale), int(max_context_len), int(partition_size), ws_ptr or None,
         ws_bytes, _dtype_code(k_cache), _stream(stream)))
+    return out
+
+
+def pa_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, group_start: torch.Tensor,
+                            prefix_lens: torch.Tensor, max_group_size: int, scale: float,
+                            max_context_len: int, partition_size: int,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """pa_decode over groups of sequences sharing a prefix in the same
+    physical blocks: ``group_start`` (int32 [num_groups + 1], runs of
+    consecutive sequences covering the batch) and ``prefix_lens`` (int32 [B],
+    shared leading tokens of each sequence, equal within a group) on the
+    device; ``max_group_size`` bounds the groups' sizes.  The shared prefix's
+    K/V is read once per group.  ``workspace`` as for pa_decode."""
+    L = _load()
+    if not getattr(L.pa_decode_shared_prefix, "argtypes", None):
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32,
+                                              i32, i32, i32, i64, ctypes.c_float, i32, i32, P,
+                                              ctypes.c_size_t, i32, P]
+        L.pa_decode_shared_prefix.restype = i32
+    dt = k_cache.dtype
+    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, dt)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                 ("group_start", group_start), ("prefix_lens", prefix_lens)):
+        _cuda(n, t, torch.int32)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, d = query.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("out/query/cache shapes disagree")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    if prefix_lens.numel() != B or group_start.dim() != 1 or group_start.numel() < 2:
+        raise ValueError("prefix_lens must be [B] and group_start [num_groups + 1]")
+    need = pa_decode_workspace_size(B, Hq, d, max_context_len, partition_size)
+    ws_ptr, ws_bytes = 0, 0
+    if need:
+        if workspace is None:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=query.device)
+        _cuda("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check("pa_decode_shared_prefix", L.pa_decode_shared_prefix(
+        out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
+        group_start.data_ptr(), prefix_lens.data_ptr(), group_start.numel() - 1,
+        int(max_group_size), B, Hq, Hkv, d, bs, NB, float(scale), int(max_context_len),
+        int(partition_size), ws_ptr or None, ws_bytes, _dtype_code(k_cache), _stream(stream)))
     return out
 
 

@@ -76,7 +76,7 @@ constexpr int32_t kMaxFusedParts = 32;
 
 extern "C" {
 
-int32_t pa_version(void) { return 2; }
+int32_t pa_version(void) { return 3; }
 
 const char *pa_status_string(int32_t status) {
   switch (status) {
@@ -232,21 +232,40 @@ int32_t pa::decode_check_args(const void *out, const void *query, const void *k_
 
 namespace {
 
+// The groups of pa_decode_shared_prefix (device arrays and their host-side bounds).
+struct SharedPrefix {
+  const int32_t *group_start, *prefix_lens;
+  int32_t num_groups, max_group_size;
+};
+
 pa_status decode_impl(void *out, const void *query, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, int32_t max_blocks_per_seq,
                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                       int64_t num_blocks, float scale, int32_t max_context_len,
                       int32_t partition_size, void *workspace, size_t workspace_bytes,
-                      int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream) {
+                      int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream,
+                      const SharedPrefix *sp = nullptr) {
   const int32_t st = pa::decode_check_args(
       out, query, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, max_context_len,
       partition_size, dtype);
-  if (st != PA_OK || num_seqs == 0) return static_cast<pa_status>(st);
+  if (st != PA_OK) return static_cast<pa_status>(st);
   const int32_t group = num_q_heads / num_kv_heads;
-  const int64_t pool_rows = num_blocks * num_kv_heads * block_size;
   const int32_t P = num_partitions(max_context_len, partition_size);
+  int32_t chunks = 0;
+  if (sp) {
+    if (!sp->group_start || !sp->prefix_lens || sp->num_groups < 1 || sp->max_group_size < 1 ||
+        partition_size <= 0 || (num_seqs > 0 && (sp->num_groups > num_seqs ||
+                                                 sp->max_group_size > num_seqs)))
+      return PA_ERR_INVALID_ARG;
+    if (kv_fp8 || partition_size > pa::kMaxSharedPrefixPartition) return PA_ERR_UNSUPPORTED;
+    const int32_t mpc = pa::shared_prefix_members_per_cta(group);
+    chunks = (sp->max_group_size + mpc - 1) / mpc;
+    if (static_cast<int64_t>(sp->num_groups) * chunks > 65535) return PA_ERR_UNSUPPORTED;
+  }
+  if (num_seqs == 0) return PA_OK;
+  const int64_t pool_rows = num_blocks * num_kv_heads * block_size;
   WsLayout w{};
   if (P > 1) {
     w = workspace_layout(static_cast<int64_t>(num_seqs) * num_q_heads, P, head_dim);
@@ -258,7 +277,7 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
 
-  pa::DecodeArgs a;
+  pa::DecodeArgs a{};
   a.out = out;
   a.query = query;
   a.block_tables = block_tables;
@@ -284,6 +303,19 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
   a.err = err;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   bool map_failed = false;
+  if (sp && P > 1) {
+    // the shared pass writes the partials of every member's shared partitions;
+    // the decode launch below computes the rest and joins them all
+    a.prefix_lens = sp->prefix_lens;
+    a.group_start = sp->group_start;
+    a.num_groups = sp->num_groups;
+    a.max_group_size = sp->max_group_size;
+    a.members_per_cta = pa::shared_prefix_members_per_cta(group);
+    a.chunks = chunks;
+    if (pa::launch_shared_prefix(a, k_cache, v_cache, pool_rows, head_dim, dtype, cs,
+                                 &map_failed) != cudaSuccess)
+      return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
+  }
   if (pa::launch_decode(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8, cs,
                         &map_failed) != cudaSuccess)
     return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
@@ -309,6 +341,23 @@ pa_status pa_decode(void *out, const void *query, const void *k_cache, const voi
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, max_context_len, partition_size, workspace,
                      workspace_bytes, dtype, false, 1.f, 1.f, stream);
+}
+
+pa_status pa_decode_shared_prefix(void *out, const void *query, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                  const int32_t *group_start, const int32_t *prefix_lens,
+                                  int32_t num_groups, int32_t max_group_size, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int64_t num_blocks, float scale,
+                                  int32_t max_context_len, int32_t partition_size,
+                                  void *workspace, size_t workspace_bytes, int32_t dtype,
+                                  void *stream) {
+  const SharedPrefix sp{group_start, prefix_lens, num_groups, max_group_size};
+  return decode_impl(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, max_context_len, partition_size, workspace,
+                     workspace_bytes, dtype, false, 1.f, 1.f, stream, &sp);
 }
 
 pa_status pa_decode_fp8(void *out, const void *query, const void *k_cache, const void *v_cache,

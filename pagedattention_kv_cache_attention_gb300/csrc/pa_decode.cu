@@ -56,33 +56,11 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_tile.cuh"
 
 namespace pa {
 
 namespace {
-
-constexpr int kTile = 16;        // tokens per sub-tile (one MMA row block)
-constexpr unsigned kFull = 0xffffffffu;
-
-// Geometry of one sub-tile in shared memory.  Rows are staged in 128-byte TMA
-// boxes (16 rows each) with the 128-byte swizzle: 16-byte unit u of row r sits
-// at unit u ^ (r & 7) of its 128-byte line.
-template <int D, bool F8> struct Shape {
-  static constexpr int kElem = F8 ? 1 : 2;               // bytes per cached element
-  static constexpr int kRowBytes = D * kElem;
-  static constexpr int kBoxElems = 128 / kElem;          // elements per 128-byte box row
-  static constexpr int kBoxes = kRowBytes / 128;         // boxes per row
-  static constexpr int kBoxBytes = kTile * 128;          // one box of 16 rows
-  static constexpr int kTileBytes = kTile * kRowBytes;   // K (or V) of one sub-tile
-  static constexpr int kQChunks = D / 32;                // 16-byte q chunks per lane
-  static constexpr int kMTiles = D / 16;                 // m16 tiles of the P.V product
-};
-
-// 16-bit caches: the 16-byte chunk (8 elements) of a head_dim row that lane
-// column c reads in QK^T step i.  Every chunk is read by exactly one (i, c);
-// chunks read by one quarter-warp in one step are all even or all odd, which
-// with the swizzle puts them in distinct banks.
-__device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 8 * (i >> 1); }
 
 // Atomic add with acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
@@ -229,6 +207,7 @@ __global__ void __launch_bounds__(NW * 32)
   int win = table_entry(lane);
 
   int ctx = a.context_lens[seq];
+  const int prefix_len = a.prefix_lens != nullptr ? a.prefix_lens[seq] : 0;
   if (ctx < 0 || ctx > (a.max_blocks_per_seq << a.bs_log2) || ctx > a.max_context_len) {
     if (threadIdx.x == 0 && part == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
     ctx = 0;
@@ -237,6 +216,11 @@ __global__ void __launch_bounds__(NW * 32)
   // partitions of this sequence that have tokens (partition 0 also stands for
   // an empty context)
   const int np_seq = ctx > 0 ? (ctx + a.part_tokens - 1) / a.part_tokens : 1;
+  // partitions [0, first) lie inside a prefix the sequence shares with its
+  // group, and the shared-prefix kernel has written their partials; the last
+  // partition always stays here, so some CTA of this grid joins
+  const int first = min(max(prefix_len, 0) / a.part_tokens, np_seq - 1);
+  if (part < first) return;
   const int t_end = min(ctx, t_begin + a.part_tokens);
   const int n_sub = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
   const int n_grp = (n_sub + NSUB - 1) / NSUB;
@@ -379,19 +363,10 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
     for (int h = 0; h < NSUB; ++h) {
       const uint8_t *Ks = stage + h * Sh::kTileBytes;
-      sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
       if constexpr (!F8) {
-#pragma unroll
-        for (int i = 0; i < Sh::kQChunks; ++i) {
-          const int ch = q_chunk(i, c);
-          const uint8_t *box = Ks + (ch >> 3) * Sh::kBoxBytes;
-          const int sw = ((ch & 7) ^ g) << 4;  // rows g and g+8 share (row & 7) = g
-          const uint4 ka = *reinterpret_cast<const uint4 *>(box + g * 128 + sw);
-          const uint4 kb = *reinterpret_cast<const uint4 *>(box + (g + 8) * 128 + sw);
-          Elem<MT>::mma(sc[h], ka.x, kb.x, ka.y, kb.y, qf[i].x, qf[i].y);
-          Elem<MT>::mma(sc[h], ka.z, kb.z, ka.w, kb.w, qf[i].z, qf[i].w);
-        }
+        qk_subtile_16<MT, D>(Ks, qf, g, c, sc[h]);
       } else {
+        sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
         // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -412,95 +387,19 @@ __global__ void __launch_bounds__(NW * 32)
 
     // ---- online softmax in base 2 (log2(e) folded into the scale), one
     // reduction over all NSUB x 16 tokens of the step
-    float x[NSUB][4];
-    float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-    for (int h = 0; h < NSUB; ++h) {
-      const bool v_lo = g < nvalid[h], v_hi = g + 8 < nvalid[h];
-      x[h][0] = v_lo ? sc[h][0] * scale_log2 : NEG_INF;
-      x[h][1] = v_lo ? sc[h][1] * scale_log2 : NEG_INF;
-      x[h][2] = v_hi ? sc[h][2] * scale_log2 : NEG_INF;
-      x[h][3] = v_hi ? sc[h][3] * scale_log2 : NEG_INF;
-      mx0 = fmaxf(mx0, fmaxf(x[h][0], x[h][2]));
-      mx1 = fmaxf(mx1, fmaxf(x[h][1], x[h][3]));
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float r0 = mn0 == NEG_INF ? 0.f : mn0;  // no valid token yet: any finite reference
-    const float r1 = mn1 == NEG_INF ? 0.f : mn1;
-    const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
     float p[NSUB][4];
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int h = 0; h < NSUB; ++h) {
-      p[h][0] = exp2f(x[h][0] - r0);
-      p[h][1] = exp2f(x[h][1] - r1);
-      p[h][2] = exp2f(x[h][2] - r0);
-      p[h][3] = exp2f(x[h][3] - r1);
-      ps0 += p[h][0] + p[h][2];
-      ps1 += p[h][1] + p[h][3];
-    }
-    l0 = l0 * al0 + ps0;
-    l1 = l1 * al1 + ps1;
-    m0 = mn0;
-    m1 = mn1;
-    if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-      for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
-    }
+    softmax_step<NSUB, Sh::kMTiles>(sc, nvalid, g, scale_log2, m0, m1, l0, l1, acc, p);
 
 #pragma unroll
     for (int h = 0; h < NSUB; ++h) {
-      // P^T as the B operand: (tokens 2c,2c+1 | 2c+8,2c+9 ; head g).  P is
-      // carried as hi + lo in the MMA type (hi = P rounded, lo = the exact fp32
-      // remainder rounded), so the P.V product keeps ~16 (bf16) or ~22 (fp16)
-      // bits of P instead of 8 or 11.
-      const uint32_t h01 = Elem<MT>::pack(p[h][0], p[h][1]);
-      const uint32_t h23 = Elem<MT>::pack(p[h][2], p[h][3]);
-      const float2 f01 = Elem<MT>::unpack(h01), f23 = Elem<MT>::unpack(h23);
-      const uint32_t pb0 = movmatrix_trans(h01);
-      const uint32_t pb1 = movmatrix_trans(h23);
-      const uint32_t pr0 = movmatrix_trans(Elem<MT>::pack(p[h][0] - f01.x, p[h][1] - f01.y));
-      const uint32_t pr1 = movmatrix_trans(Elem<MT>::pack(p[h][2] - f23.x, p[h][3] - f23.y));
+      // P^T as the B operand (tokens 2c,2c+1 | 2c+8,2c+9 ; head g), hi + lo
+      uint32_t pb0, pb1, pr0, pr1;
+      p_operands<MT>(p[h], pb0, pb1, pr0, pr1);
       const uint8_t *Vs = stage + (NSUB + h) * Sh::kTileBytes;
 
       // ---- O^T += V^T P^T : V rows 2c, 2c+1, 2c+8, 2c+9; unit g of every box
       if constexpr (!F8) {
-        uint4 v[4][Sh::kBoxes];
-#pragma unroll
-        for (int ri = 0; ri < 4; ++ri) {
-          const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
-          const bool keep = r < nvalid[h];
-#pragma unroll
-          for (int b = 0; b < Sh::kBoxes; ++b) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(Vs + b * Sh::kBoxBytes + r * 128 +
-                                                              ((g ^ (r & 7)) << 4));
-            v[ri][b] = keep ? xv : make_uint4(0, 0, 0, 0);
-          }
-        }
-#pragma unroll
-        for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-          // output dim of MMA row g is (box A, element eA) of chunk g; row g+8 is (box B, eB)
-          constexpr int bA = 0;
-          constexpr int bB = Sh::kBoxes - 1;
-          const int eA = mt;
-          const int eB = D == 128 ? mt : 4 + mt;
-          const uint32_t a0 = pair_of(v[0][bA], v[1][bA], eA);
-          const uint32_t a1 = pair_of(v[0][bB], v[1][bB], eB);
-          const uint32_t a2 = pair_of(v[2][bA], v[3][bA], eA);
-          const uint32_t a3 = pair_of(v[2][bB], v[3][bB], eB);
-          Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pb0, pb1);
-          Elem<MT>::mma(acc[mt], a0, a1, a2, a3, pr0, pr1);
-        }
+        pv_subtile_16<MT, D>(Vs, nvalid[h], g, c, pb0, pb1, pr0, pr1, acc);
       } else {
         // unit g (dims 16g .. 16g+15) of each row, still E4M3
         uint4 v8[4];
@@ -588,21 +487,8 @@ __global__ void __launch_bounds__(NW * 32)
         a.ws_l[pr1] = l1;
       }
     }
-    float *o0 = a.ws_o + pr0 * D;
-    float *o1 = a.ws_o + pr1 * D;
-#pragma unroll
-    for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-      const int dA = F8 ? 16 * g + mt : 8 * g + mt;
-      const int dB = F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
-      if (h0 < G) {
-        o0[dA] = acc[mt][0] * inv0;
-        o0[dB] = acc[mt][2] * inv0;
-      }
-      if (h1 < G) {
-        o1[dA] = acc[mt][1] * inv1;
-        o1[dB] = acc[mt][3] * inv1;
-      }
-    }
+    store_partial_o<D, F8>(a.ws_o + pr0 * D, a.ws_o + pr1 * D, h0 < G, h1 < G, acc, inv0, inv1,
+                           g);
     grid_launch_dependents();
     return;
   }
@@ -619,8 +505,8 @@ __global__ void __launch_bounds__(NW * 32)
   }
 #pragma unroll
   for (int mt = 0; mt < Sh::kMTiles; ++mt) {
-    const int dA = F8 ? 16 * g + mt : 8 * g + mt;
-    const int dB = F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
+    const int dA = pv_dim_a<D, F8>(g, mt);
+    const int dB = pv_dim_b<D, F8>(g, mt);
     float *h0 = wacc + (warp * 8 + 2 * c) * D;
     float *h1 = h0 + D;
     h0[dA] = acc[mt][0];
@@ -670,7 +556,8 @@ __global__ void __launch_bounds__(NW * 32)
   }
   if (a.fuse_join && np_seq > 1) {
     // count this partition in; the CTA that completes the count joins them
-    // all.  The barrier orders every thread's partial stores before thread 0's
+    // all (with a shared prefix, the partials of partitions below `first`
+    // come from the shared-prefix grid, which finished before this one began).  The barrier orders every thread's partial stores before thread 0's
     // acquire-release add, which publishes them (release, cumulative) and, for
     // the last CTA, makes every other CTA's partials visible (acquire).
     __syncthreads();
@@ -679,10 +566,11 @@ __global__ void __launch_bounds__(NW * 32)
       unsigned *cnt = a.ws_cnt + static_cast<int64_t>(seq) * a.num_kv_heads + kvh;
       const unsigned prev = atom_add_acq_rel_gpu(cnt, kJoinArrive);
       const unsigned k = prev & 0xffffu;
+      const unsigned arrivals = static_cast<unsigned>(np_seq - first);  // CTAs that count in
       uint32_t last = 0;
-      if ((prev >> 16) != k || k >= static_cast<unsigned>(np_seq)) {
+      if ((prev >> 16) != k || k >= arrivals) {
         atomicOr(a.err, kErrWorkspace);  // the counter did not start at zero
-      } else if (k == static_cast<unsigned>(np_seq - 1)) {
+      } else if (k == arrivals - 1) {
         last = 1;
         atomicExch(cnt, 0u);  // every partition has arrived: ready for the next call
       }

@@ -18,6 +18,7 @@ constexpr unsigned kErrBadSlot = 2u;
 constexpr unsigned kErrBadLen = 4u;
 constexpr unsigned kErrTimeout = 8u;
 constexpr unsigned kErrWorkspace = 16u;
+constexpr unsigned kErrPrefix = 32u;
 
 // Longest a warp waits for one staged tile before it gives up (ns).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;

@@ -2,6 +2,7 @@
 // translation units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,6 +58,14 @@ struct DecodeArgs {
   unsigned *ws_cnt;             // join counters, one per (sequence, KV head) (num_parts > 1)
   int fuse_join;                // 1: the last partition CTA of a (sequence, KV head) joins
   unsigned *err;                // device error word
+  // Shared-prefix decode (nullptr / unused otherwise).  prefix_lens [B]:
+  // leading tokens of each sequence held in the same physical blocks as the
+  // rest of its group; group_start [num_groups + 1]: the groups are runs of
+  // consecutive sequences.
+  const int32_t *prefix_lens;
+  const int32_t *group_start;
+  int num_groups, max_group_size;
+  int members_per_cta, chunks;  // sequences per shared-prefix CTA, CTAs per group
 };
 
 struct ReduceArgs {
@@ -128,11 +137,27 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Largest partition size the shared-prefix kernel takes (its shared-memory
+// table holds one pool row per 16-token sub-tile of a partition).
+constexpr int kMaxSharedPrefixPartition = 8192;
+
+// The pool viewed as a 2-D tensor [num_blocks * num_kv_heads * block_size
+// rows, head_dim] for TMA loads of 16-row, 128-byte boxes (128-byte swizzle).
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
+                     bool fp8);
+
 // kv_fp8: the caches hold FP8 E4M3 codes (queries and output fp16).
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
                           cudaStream_t stream, bool *map_failed);
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
+// The shared-prefix pass of pa_decode_shared_prefix (16-bit caches); the
+// decode launch with a.prefix_lens set follows it on the same stream.
+cudaError_t launch_shared_prefix(const DecodeArgs &a, const void *k_cache, const void *v_cache,
+                                 int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                                 bool *map_failed);
+// Sequences of one group that a shared-prefix CTA serves at query group size G.
+int shared_prefix_members_per_cta(int group);
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
 cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,

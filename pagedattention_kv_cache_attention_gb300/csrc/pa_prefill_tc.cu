@@ -678,9 +678,6 @@ cudaError_t launch_prefill_tc_d(const PrefillArgs &a, const CUtensorMap &km,
 
 }  // namespace
 
-bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
-                     bool fp8);
-
 // Every shape pa_prefill accepts runs here.  Chunks that fill more than one
 // 128-row tile run with two tiles per CTA (one CTA per SM); shorter ones
 // (short chunks, decode-like rows) with one tile per CTA, two CTAs per SM.

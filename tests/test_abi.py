@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
-    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 2 ? 0 : 1;}\n')
+    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 3 ? 0 : 1;}\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
                     "-I", os.path.join(ROOT, "include"), str(src)], check=True)
 
@@ -118,3 +118,36 @@ def test_reshape_host_validation(lib):
     assert call(sm=None) == 1
     assert call(kc=P(0x10002)) == 1
     assert call(dt=3) == 1
+
+
+def test_version(lib):
+    assert lib.pa_version() == 3
+
+
+def _shared_prefix_status(lib, **over):
+    P = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    fake = P(0x10000)  # never dereferenced: every case below fails host checks first
+    args = dict(out=fake, query=fake, k=fake, v=fake, bt=fake, mb=160, cl=fake, gs=fake, pl=fake,
+                ng=4, mgs=8, B=32, Hq=32, Hkv=8, d=128, bs=16, NB=4096, scale=0.088, maxctx=2560,
+                ps=512, ws=fake, wsb=1 << 30, dt=0, st=None)
+    args.update(over)
+    lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i32,
+                                            i32, i32, ctypes.c_int64, ctypes.c_float, i32, i32, P,
+                                            ctypes.c_size_t, i32, P]
+    return lib.pa_decode_shared_prefix(*args.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(gs=None), 1), (dict(pl=None), 1),                 # group arrays missing
+    (dict(ng=0), 1), (dict(ng=33), 1),                      # 1 <= num_groups <= num_seqs
+    (dict(mgs=0), 1), (dict(mgs=33), 1),                    # 1 <= max_group_size <= num_seqs
+    (dict(ps=0), 1),                                        # sharing needs partitions
+    (dict(ps=16384, maxctx=65536), 2),                      # partition beyond the kernel's table
+    (dict(d=96), 2), (dict(ps=24), 1),                      # pa_decode's own checks come first
+    (dict(B=65535, ng=65535, mgs=16, NB=1 << 16, Hkv=1, Hq=4, bs=16), 2),  # grid z too large
+    (dict(ws=None, wsb=0), 1),                              # a split needs a workspace
+    (dict(B=0, ng=1, mgs=1), 0),                            # empty batch: nothing to do
+])
+def test_shared_prefix_host_validation(lib, over, status):
+    assert _shared_prefix_status(lib, **over) == status

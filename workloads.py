@@ -61,6 +61,12 @@ class Workload:
     kv_dtype: str = ""              # "" = same as dtype; "e4m3": uint8 FP8 caches
     k_scale: float = 1.0            # FP8 caches: code e stands for k_scale * e
     v_scale: float = 1.0
+    # prefix sharing (copy-on-write batches): groups are runs of consecutive
+    # sequences, group g = sequences group_start[g] .. group_start[g+1]-1;
+    # prefix_lens[i] = leading tokens of sequence i held in blocks shared with
+    # its whole group (None: no sharing described)
+    group_start: Optional[torch.Tensor] = None   # int32 [num_groups + 1]
+    prefix_lens: Optional[torch.Tensor] = None   # int32 [B]
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -138,8 +144,15 @@ class Workload:
         w = self.clone()
         w.k_cache, w.v_cache, w.num_blocks = kc, vc, nb
         w.block_tables = torch.from_numpy(bt)
+        w.group_start = w.prefix_lens = None  # nothing is shared any more
         # the new token's slot is always in a private block, so slots stay valid
         return w
+
+    @property
+    def max_group_size(self) -> int:
+        if self.group_start is None:
+            return 1
+        return int((self.group_start[1:] - self.group_start[:-1]).max().item())
 
 
 def _poison(t: torch.Tensor, dtype: str) -> None:
@@ -217,13 +230,27 @@ def _build(name, seed, dtype, B, Hq, Hkv, d, bs, ctx: np.ndarray, pool_slack: fl
     value = _randn((B, Hkv, d), gen, dtype)
     scale = float(np.float32(1.0 / math.sqrt(d)))
     check_distinct_slots(slots)
+    group_start = prefix_lens = None
+    if prefix_groups:
+        # every sequence in one run of consecutive sequences (a sequence in no
+        # listed group is a group of its own, sharing nothing)
+        starts, pl = [0], np.zeros(B, dtype=np.int32)
+        for i in range(1, B + 1):
+            if i == B or group_of.get(i, -1 - i) != group_of.get(i - 1, -2 - i):
+                starts.append(i)
+        for g in prefix_groups:
+            if sorted(g) != list(range(min(g), max(g) + 1)):
+                raise ValueError("prefix groups must be runs of consecutive sequences")
+            pl[g] = shared_full * bs
+        group_start = torch.tensor(starts, dtype=torch.int32)
+        prefix_lens = torch.from_numpy(pl)
     return Workload(name=name, dtype=dtype, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,
                     head_dim=d, block_size=bs, num_blocks=NB, scale=scale,
                     partition_size=partition_size,
                     context_lens=torch.from_numpy(ctx.astype(np.int32)),
                     block_tables=torch.from_numpy(bt), slot_mapping=torch.from_numpy(slots),
                     query=query, key=key, value=value, k_cache=k_cache, v_cache=v_cache,
-                    seed=seed)
+                    seed=seed, group_start=group_start, prefix_lens=prefix_lens)
 
 
 def check_distinct_slots(slots) -> None:
