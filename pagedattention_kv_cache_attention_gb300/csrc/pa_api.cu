@@ -262,7 +262,7 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
     if (kv_fp8 || partition_size > pa::kMaxSharedPrefixPartition) return PA_ERR_UNSUPPORTED;
     const int32_t mpc = pa::shared_prefix_members_per_cta(group);
     chunks = (sp->max_group_size + mpc - 1) / mpc;
-    if (static_cast<int64_t>(sp->num_groups) * chunks > 65535) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(P) * chunks > 0x7fffffff) return PA_ERR_UNSUPPORTED;
   }
   if (num_seqs == 0) return PA_OK;
   const int64_t pool_rows = num_blocks * num_kv_heads * block_size;

@@ -181,8 +181,13 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncwarp();
 
-  // inputs (the pool above all) may come from the kernel launched just before
-  grid_dependency_wait();
+  // inputs (the pool above all) may come from the kernel launched just before.
+  // After the shared-prefix kernel (launched between the scatter and this
+  // grid) the wait moves to the epilogue: that kernel lets this grid start
+  // once each of its CTAs has itself waited for the scatter, so the pool is
+  // complete here, and only the join needs its partials.
+  const bool after_shared_pass = a.prefix_lens != nullptr;
+  if (!after_shared_pass) grid_dependency_wait();
 
   // Step k of warp w covers sub-tiles (w + k NW) NSUB + h, h < NSUB, of the
   // partition (WP: sub-tiles k NSUB + h of the warp's own partition).  A
@@ -461,6 +466,9 @@ __global__ void __launch_bounds__(NW * 32)
     for (int kk = k_stop; kk < min(k_stop + S, my_n); ++kk)
       (void)mbar_wait_bounded(&my_bars[kk % S], (kk / S) & 1);
   }
+  // the shared-prefix grid's partials are complete from here on (and this
+  // grid's completion implies that grid's, for the reduce launched after it)
+  if (after_shared_pass) grid_dependency_wait();
 
   // per-warp row sums over the 8 token rows (lanes differing in g)
 #pragma unroll

@@ -145,7 +145,8 @@ def _shared_prefix_status(lib, **over):
     (dict(ps=0), 1),                                        # sharing needs partitions
     (dict(ps=16384, maxctx=65536), 2),                      # partition beyond the kernel's table
     (dict(d=96), 2), (dict(ps=24), 1),                      # pa_decode's own checks come first
-    (dict(B=65535, ng=65535, mgs=16, NB=1 << 16, Hkv=1, Hq=4, bs=16), 2),  # grid z too large
+    (dict(B=65535, ng=1, mgs=65535, Hq=8, Hkv=1, maxctx=1 << 30, ps=16, mb=1 << 26),
+     2),                                                    # grid x too large
     (dict(ws=None, wsb=0), 1),                              # a split needs a workspace
     (dict(B=0, ng=1, mgs=1), 0),                            # empty batch: nothing to do
 ])
