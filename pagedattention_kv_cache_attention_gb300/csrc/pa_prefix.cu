@@ -301,14 +301,14 @@ __global__ void __launch_bounds__(kPxWarps * 32)
       const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
       const float rA = nA == -INFINITY ? 0.f : nA;  // any finite reference
       const float rB = nB == -INFINITY ? 0.f : nB;
-      const float alA = exp2f(mA - rA), alB = exp2f(mB - rB);
+      const float alA = softmax_exp2(mA - rA), alB = softmax_exp2(mB - rB);
       float pr[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        pr[j][0] = exp2f(x[j][0] - rA);
-        pr[j][1] = exp2f(x[j][1] - rA);
-        pr[j][2] = exp2f(x[j][2] - rB);
-        pr[j][3] = exp2f(x[j][3] - rB);
+        pr[j][0] = softmax_exp2(x[j][0] - rA);
+        pr[j][1] = softmax_exp2(x[j][1] - rA);
+        pr[j][2] = softmax_exp2(x[j][2] - rB);
+        pr[j][3] = softmax_exp2(x[j][3] - rB);
       }
       lA = lA * alA + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
       lB = lB * alB + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);

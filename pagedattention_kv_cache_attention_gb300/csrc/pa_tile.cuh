@@ -82,6 +82,12 @@ __device__ __forceinline__ void qk_subtile_16(const uint8_t *Ks, const uint4 (&q
   }
 }
 
+// 2^x for the softmax probabilities and rescale factors: the PTX approximate
+// base-2 exponential (relative error near 2^-22; results below 2^-126 flush
+// to zero, i.e. probabilities that small relative to the running maximum are
+// dropped, far below what the fp32 accumulation resolves).  2^-inf = 0.
+__device__ __forceinline__ float softmax_exp2(float x) { return ex2_approx(x); }
+
 // One online-softmax step in base 2 (log2(e) is folded into scale_log2) over
 // the NSUB sub-tiles of a pipeline step, for the lane's columns 2c (m0, l0)
 // and 2c + 1 (m1, l1): tokens at or past nvalid[h] of sub-tile h get logit
@@ -115,14 +121,14 @@ __device__ __forceinline__ void softmax_step(const float (&sc)[NSUB][4], const i
   const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
   const float r0 = mn0 == NEG_INF ? 0.f : mn0;  // no valid token yet: any finite reference
   const float r1 = mn1 == NEG_INF ? 0.f : mn1;
-  const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
+  const float al0 = softmax_exp2(m0 - r0), al1 = softmax_exp2(m1 - r1);
   float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
   for (int h = 0; h < NSUB; ++h) {
-    p[h][0] = exp2f(x[h][0] - r0);
-    p[h][1] = exp2f(x[h][1] - r1);
-    p[h][2] = exp2f(x[h][2] - r0);
-    p[h][3] = exp2f(x[h][3] - r1);
+    p[h][0] = softmax_exp2(x[h][0] - r0);
+    p[h][1] = softmax_exp2(x[h][1] - r1);
+    p[h][2] = softmax_exp2(x[h][2] - r0);
+    p[h][3] = softmax_exp2(x[h][3] - r1);
     ps0 += p[h][0] + p[h][2];
     ps1 += p[h][1] + p[h][3];
   }
