@@ -4,8 +4,8 @@ CPU oracle.
 The oracle knows nothing of prefix groups: it attends every sequence over its
 own tokens through its own block table, exactly as for pa_decode.  The shared
 pass must therefore reproduce per-sequence attention while reading each group's
-shared prefix once.  Cases span several partitions, group chunks (groups larger
-than one CTA's 32 query columns), members shorter than the shared prefix,
+shared prefix once.  Cases span several partitions, group chunks (groups with
+more than one CTA's 16 query rows), members shorter than the shared prefix,
 partitions joined inside the decode kernel and by the reduce kernel, and the
 device-side checks of the group description.
 """
@@ -110,6 +110,8 @@ CASES = [
     (4, 3, 40, 16, 16, 32, 8, 128, 16, "fp16"),      # partial prefix block (copied, not shared)
     (2, 3, 64, 8, 64, 32, 8, 128, 16, "bf16"),       # prefix = one partition
     (5, 1, 128, 40, 32, 32, 8, 128, 16, "fp16"),     # groups of one
+    (2, 7, 144, 30, 48, 40, 8, 128, 16, "bf16"),     # G 5 (15 of 16 rows); 3 sub-tiles per partition
+    (3, 5, 112, 24, 16, 56, 8, 64, 32, "fp16"),      # G 7 (14 rows), one sub-tile per partition
 ]
 
 
@@ -146,6 +148,16 @@ def test_many_partitions_join_in_the_reduce_kernel(pa):
     assert pa.pa_decode_num_partitions(r.maxctx, 32) > 32
     assert r.err == 0
     r.check("reduce-kernel join")
+
+
+def test_loose_group_size_bound(pa):
+    """max_group_size above every group's size: the extra chunks find no
+    members and leave."""
+    w = W.make("shared_prefix_cow", seed=13, groups=3, group_size=3, prefix_len=128, max_len=40,
+               partition_size=32)
+    r = SharedRun(pa, w, 32, max_group_size=w.num_seqs)
+    assert r.err == 0
+    r.check("loose group-size bound")
 
 
 def test_zero_prefix_is_plain_decode(pa):
