@@ -50,3 +50,32 @@ def test_prefill_flops_by_hand():
     # seq 0: positions 7, 8, 9 -> 8 + 9 + 10 keys; seq 1: positions 0..3 -> 1+2+3+4 keys
     keys = (8 + 9 + 10) + (1 + 2 + 3 + 4)
     assert bench.prefill_flops(pw) == 4 * 64 * 4 * keys
+
+
+def test_shared_prefix_groups_and_unique_bytes_by_hand():
+    """The copy-on-write batch records its groups (runs of consecutive
+    sequences) and each sequence's shared prefix (whole shared blocks only: a
+    partial last prefix block is copied per sequence, so it is not shared);
+    the distinct-slot byte count takes each group's shared rows once."""
+    ng, gs, P, bs = 3, 4, 40, 16
+    w = W.make("shared_prefix_cow", 2, groups=ng, group_size=gs, prefix_len=P, max_len=30,
+               num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=bs)
+    assert w.group_start.tolist() == [0, 4, 8, 12]
+    shared = (P // bs) * bs                                  # 32 tokens in shared blocks
+    assert w.prefix_lens.tolist() == [shared] * (ng * gs)
+    assert w.max_group_size == gs
+    bt = w.block_tables.numpy()
+    for g in range(ng):
+        rows = bt[g * gs:(g + 1) * gs, : P // bs]
+        assert (rows == rows[0]).all()                       # the group's shared blocks
+        assert len(set(bt[g * gs:(g + 1) * gs, P // bs].tolist())) == gs   # copied block
+    ctx = w.context_lens.numpy().astype(np.int64)
+    unique_tokens = ng * shared + int((ctx - shared).sum())
+    ab = bench.algorithmic_bytes(w)
+    assert ab["kv_unique"] == 2 * unique_tokens * 2 * 64 * 2
+    assert ab["kv"] == 2 * int(ctx.sum()) * 2 * 64 * 2
+    assert ab["decode_unique"] == ab["kv_unique"] + ab["qo"] + ab["tables"]
+    # layout changes keep or drop the description consistently
+    assert w.permuted(1).group_start.tolist() == [0, 4, 8, 12]
+    assert w.unshared().group_start is None and w.unshared().prefix_lens is None
+    assert "kv_unique" not in bench.algorithmic_bytes(W.make("tiny_mha", 0))
