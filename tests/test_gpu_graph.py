@@ -136,3 +136,69 @@ def test_captured_step_replays_bitwise(pa, fp8):
     assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16))
     assert torch.equal(bits(static["kc"]), bits(kc)) and torch.equal(bits(static["vc"]), bits(vc))
     assert_matches_oracle(static, other, fp8, "replay with new inputs")
+
+
+def test_captured_shared_prefix_step(pa):
+    """The copy-on-write step through pa_decode_shared_prefix (scatter, the
+    shared pass, the decode and its join) captured once and replayed with a
+    second batch of the same shapes written into the captured buffers: the
+    same bits as the eager calls, and the oracle's per-sequence attention."""
+    kw = dict(groups=4, group_size=4, prefix_len=256, max_len=64, partition_size=64)
+    base = W.make("shared_prefix_cow", 53, **kw)
+    other = W.make("shared_prefix_cow", 54, **kw)
+    assert torch.equal(base.group_start, other.group_start)
+    dev = torch.device("cuda")
+    maxctx = max(base.max_context_len, other.max_context_len)
+    NB = max(base.num_blocks, other.num_blocks)
+    ps, mgs = 64, base.max_group_size
+
+    def buffers(w):
+        kc = torch.zeros((NB,) + tuple(w.k_cache.shape[1:]), dtype=w.k_cache.dtype, device=dev)
+        vc = torch.zeros_like(kc)
+        kc[:w.num_blocks] = w.k_cache.to(dev)
+        vc[:w.num_blocks] = w.v_cache.to(dev)
+        return dict(kc=kc, vc=vc, key=w.key.to(dev), value=w.value.to(dev),
+                    sm=w.slot_mapping.to(dev), q=w.query.to(dev), bt=w.block_tables.to(dev),
+                    cl=w.context_lens.to(dev), gs=w.group_start.to(dev),
+                    pl=w.prefix_lens.to(dev), out=torch.empty_like(w.query, device=dev))
+
+    ws = pa.new_decode_workspace(base.num_seqs, base.num_q_heads, base.head_dim, maxctx, ps)
+
+    def step(b, w, stream=None):
+        pa.pa_reshape_and_cache(b["key"], b["value"], b["kc"], b["vc"], b["sm"], stream=stream)
+        pa.pa_decode_shared_prefix(b["out"], b["q"], b["kc"], b["vc"], b["bt"], b["cl"], b["gs"],
+                                   b["pl"], mgs, w.scale, maxctx, ps, workspace=ws,
+                                   stream=stream)
+
+    eager = {}
+    for name, w in (("base", base), ("other", other)):
+        b = buffers(w)
+        step(b, w)
+        torch.cuda.synchronize()
+        eager[name] = (b["out"].clone(), b["kc"].clone(), b["vc"].clone())
+
+    static = buffers(base)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(static, base, stream=side)        # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    fresh = buffers(base)
+    for k in ("kc", "vc"):
+        static[k].copy_(fresh[k])
+    with torch.cuda.graph(g):
+        step(static, base, stream=torch.cuda.current_stream())
+    for name, w, copy_in in (("base", base, False), ("other", other, True)):
+        if copy_in:
+            nb = buffers(w)
+            for k in ("kc", "vc", "key", "value", "sm", "q", "bt", "cl", "gs", "pl"):
+                static[k].copy_(nb[k])
+        g.replay()
+        torch.cuda.synchronize()
+        assert pa.pa_device_errors() == 0
+        out, kc, vc = eager[name]
+        assert torch.equal(static["out"].view(torch.int16), out.view(torch.int16)), name
+        assert torch.equal(bits(static["kc"]), bits(kc)) and torch.equal(bits(static["vc"]), bits(vc))
+        assert_matches_oracle(static, w, False, f"shared-prefix replay ({name})")
