@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpa.so")
 SOURCES = ("pa_api.cu", "pa_blocks.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill_tc.cu",
-           "pa_prefix.cu", "pa_static_ws.cu")
+           "pa_static_ws.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

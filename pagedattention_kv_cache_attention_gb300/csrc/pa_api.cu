@@ -442,7 +442,7 @@ pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
     return PA_ERR_UNSUPPORTED;
   unsigned int *err = nullptr;
   if (error_word(&err) != cudaSuccess) return PA_ERR_CUDA;
-  pa::PrefillArgs a;
+  pa::PrefillArgs a{};
   a.out = out;
   a.query = query;
   a.query_start = query_start;

@@ -106,6 +106,15 @@ struct PrefillArgs {
   int64_t num_blocks;
   float scale_log2;
   unsigned *err;
+  // The shared-prefix pass (the same kernel over a group's shared prefix):
+  // rows are (member, query head) pairs of a group's sequences, keys the
+  // partition [p part_tokens, (p + 1) part_tokens) read through the first
+  // taking member's table, and each taking member's rows are written as split
+  // partials (m, l, o) into the decode workspace.  Unused by pa_prefill.
+  float *ws_m, *ws_l, *ws_o;
+  const int32_t *prefix_lens, *group_start;
+  int num_groups, max_group_size, members_per_cta, chunks;
+  int part_tokens, num_parts, max_context_len;
 };
 
 struct BlockCopyArgs {

@@ -124,11 +124,12 @@ struct PairLayout {
   static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
 };
 
-template <typename T, int D, int SK, int SV, bool SPLIT, int TILES>
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX>
 __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
+  static_assert(!PX || TILES == 1, "the shared-prefix pass runs one tile per CTA");
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   using L = PairLayout<SK, SV, TILES, D>;
   constexpr int kAtoms = L::kAtoms;
@@ -158,10 +159,14 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   uint64_t *q_ready = pv_done + 4;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
 
-  const int tile = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.group;
-  const int tpc = TILES * kTcRows / G; // tokens per CTA
+  const int tpc = TILES * kTcRows / G; // tokens per CTA (members, in the shared-prefix pass)
+  // shared-prefix pass: first_m of each member of the CTA, then the source
+  // member, the member count and the first member's sequence
+  int *px_first = reinterpret_cast<int *>(tmem_slot + 4);
+  int *px_ctl = px_first + kTcRows;
 
   if (tid == 0) {
     for (int s = 0; s < SK; ++s) {
@@ -191,30 +196,109 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   const uint32_t tmem = *tmem_slot;
   grid_dependency_wait();  // the chunk's K/V may come from the kernel before
 
-  const int q0 = a.query_start[seq];
-  const int q_len = a.query_start[seq + 1] - q0;
-  const int ctx = a.context_lens[seq];
+  // Rows are (token, head) pairs of one chunk -- in the shared-prefix pass
+  // (member, head) pairs of consecutive sequences, whose queries sit exactly
+  // where a chunk's tokens would -- and keys run over [key_base, key_base +
+  // n_keys) of the sequence's (the source member's) table.
+  int q0, q_len, t_first, t_last, base_pos, n_keys, key_base = 0, px_p = 0;
   bool active = true;
-  if (q_len < 0 || ctx < q_len || ctx > (a.max_blocks_per_seq << a.bs_log2) ||
-      q_len > a.max_q_len) {
-    if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
-    active = false;
+  const int32_t *bt_row;
+  if constexpr (PX) {
+    // the decode grid after this one may start now: it streams the
+    // sequences' own partitions meanwhile and waits for these partials only
+    // before it joins them
+    grid_launch_dependents();
+    const int grp = blockIdx.z, chunk = blockIdx.x % a.chunks;
+    px_p = blockIdx.x / a.chunks;
+    const int P = a.part_tokens;
+    if (warp == 0) {
+      const int g0 = a.group_start[grp], g1 = a.group_start[grp + 1];
+      const bool group_ok = g0 >= 0 && g1 >= g0 && g1 <= a.num_seqs &&
+                            g1 - g0 <= a.max_group_size && (grp > 0 || g0 == 0) &&
+                            (grp < a.num_groups - 1 || g1 == a.num_seqs);
+      const bool reporter = px_p == 0 && kvh == 0;  // one CTA per chunk reports bad input
+      if (!group_ok && reporter && chunk == 0 && lane == 0) atomicOr(a.err, kErrPrefix);
+      const int m0 = g0 + chunk * a.members_per_cta;
+      const int nm = group_ok ? max(0, min(a.members_per_cta, g1 - m0)) : 0;
+      int src = -1;
+      for (int i0 = 0; i0 < nm; i0 += 32) {
+        const int i = i0 + lane;
+        int first = 0;
+        if (i < nm) {
+          int c = a.context_lens[m0 + i];
+          // the decode kernel flags a bad length; here it only means "nothing shared"
+          if (c < 0 || c > (a.max_blocks_per_seq << a.bs_log2) || c > a.max_context_len) c = 0;
+          const int np = c > 0 ? (c + P - 1) / P : 1;
+          const int pl = a.prefix_lens[m0 + i];
+          if (pl != a.prefix_lens[g0] && reporter) atomicOr(a.err, kErrPrefix);
+          first = min(max(pl, 0) / P, np - 1);
+          px_first[i] = first;
+        }
+        const unsigned takers = __ballot_sync(kFullMask, i < nm && px_p < first);
+        if (src < 0 && takers) src = i0 + __ffs(takers) - 1;
+      }
+      if (lane == 0) {
+        px_ctl[0] = src;
+        px_ctl[1] = nm;
+        px_ctl[2] = m0;
+      }
+    }
+    __syncthreads();
+    const int src = px_ctl[0], nm = px_ctl[1];
+    q0 = px_ctl[2];
+    active = src >= 0;  // some member takes this partition from here
+    q_len = nm;
+    t_first = 0;
+    t_last = nm - 1;
+    base_pos = 0;
+    n_keys = P;
+    key_base = px_p * P;
+    // p < first_src <= np_src - 1: the partition ends inside the source's
+    // context, so every table entry it needs is inside the source's row
+    bt_row = a.block_tables + static_cast<int64_t>(q0 + max(src, 0)) * a.max_blocks_per_seq;
+    if (active && kvh == 0) {
+      // every other taker must reference the same blocks (checked once per
+      // partition; it only sets a flag)
+      const int lb0 = key_base >> a.bs_log2;
+      const int nlb = ((key_base + P - 1) >> a.bs_log2) - lb0 + 1;
+      for (int it = tid; it < nm * nlb; it += blockDim.x) {
+        const int i = it / nlb, lb = lb0 + it % nlb;
+        if (i != src && px_p < px_first[i] &&
+            a.block_tables[static_cast<int64_t>(q0 + i) * a.max_blocks_per_seq + lb] !=
+                bt_row[lb])
+          atomicOr(a.err, kErrPrefix);
+      }
+    }
+  } else {
+    const int tile = blockIdx.x, seq = blockIdx.z;
+    q0 = a.query_start[seq];
+    q_len = a.query_start[seq + 1] - q0;
+    const int ctx = a.context_lens[seq];
+    if (q_len < 0 || ctx < q_len || ctx > (a.max_blocks_per_seq << a.bs_log2) ||
+        q_len > a.max_q_len) {
+      if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.err, kErrBadLen);
+      active = false;
+    }
+    t_first = tile * tpc;
+    if (t_first >= q_len) active = false;
+    t_last = min(q_len, t_first + tpc) - 1;
+    base_pos = ctx - q_len;
+    n_keys = base_pos + t_last + 1;
+    bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
   }
-  const int t_first = tile * tpc;
-  if (t_first >= q_len) active = false;
-  const int t_last = min(q_len, t_first + tpc) - 1;
-  const int base_pos = ctx - q_len;
   // per tile: last token (-1 when the tile has no rows) and step count; tile 1
   // holds the later tokens, so it reads every step tile 0 reads.  Tile 0's
   // rows reach token (kTcRows - 1) / G; tile 1's begin at token kTcRows / G.
+  // (The shared-prefix pass has no causal limit: every row sees all n_keys.)
   const int last0 = min(t_last, t_first + (kTcRows - 1) / G);
   const int last1 = TILES == 2 && t_first + kTcRows / G <= t_last ? t_last : -1;
-  const int n_keys = base_pos + t_last + 1;
-  const int n_steps0 = active ? (base_pos + last0 + 1 + kPairKeys - 1) / kPairKeys : 0;
+  const int n_steps0 =
+      active ? ((PX ? n_keys : base_pos + last0 + 1) + kPairKeys - 1) / kPairKeys : 0;
   const int n_steps1 = active && last1 >= 0 ? (n_keys + kPairKeys - 1) / kPairKeys : 0;
   const int n_steps = max(n_steps0, n_steps1);
-  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
   const int n_sub = (n_keys + 15) / 16;
+  // table entry of the 16-key sub-tile u of the key range
+  auto table_entry = [&](int u) { return bt_row[(key_base + u * 16) >> a.bs_log2]; };
 
   if (active && warp < kIssue0) {
     // ------------------------------------------------------------ softmax warps
@@ -223,7 +307,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     const int rc = t * kTcRows + r;                    // row within the CTA
     const int tok = t_first + rc / G;
     const bool row_ok = tok <= t_last;
-    const int pos = base_pos + tok;
+    const int pos = PX ? n_keys - 1 : base_pos + tok;  // keys up to pos are attended to
     const int my_steps = t == 0 ? n_steps0 : n_steps1;
     {
       const T *qrow = static_cast<const T *>(a.query) +
@@ -246,7 +330,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       const int u = n * kSub + lane;
       bool ok = false;
       if (lane < kSub && u < n_sub) {
-        const int phys = bt_row[(u * 16) >> a.bs_log2];
+        const int phys = table_entry(u);
         ok = phys >= 0 && static_cast<int64_t>(phys) < a.num_blocks;
       }
       return __ballot_sync(kFullMask, ok) & kAllSub;
@@ -284,7 +368,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       int bt_next = -1;
       {
         const int u = (n + 1) * kSub + lane;
-        if (n + 1 < my_steps && lane < kSub && u < n_sub) bt_next = bt_row[(u * 16) >> a.bs_log2];
+        if (n + 1 < my_steps && lane < kSub && u < n_sub) bt_next = table_entry(u);
       }
       const int key0 = n * kPairKeys;
       const bool full_step = row_ok && key0 + kPairKeys - 1 <= pos && vmask == kAllSub;
@@ -389,8 +473,34 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       if (__all_sync(kFullMask, mbar_wait_bounded(&pv_done[2 * t + last % kPBufs], (last / kPBufs) & 1))) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        T *orow = static_cast<T *>(a.out) +
-                  (static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G) * D;
+        const int64_t orow_idx = static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G;
+        if constexpr (PX) {
+          // the partition's partial of this row, for a member that takes the
+          // partition from here: (m, l) with the row's running reference
+          // max and o = O / l
+          // (the TMEM loads are warp-wide; only the stores depend on the row)
+          const bool takes = row_ok && px_p < px_first[tok];
+          const int64_t pr = orow_idx * a.num_parts + px_p;
+          if (takes) {
+            a.ws_m[pr] = m_ref;
+            a.ws_l[pr] = l;
+          }
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            float o[32];
+            tmem_ld32(lane_addr + kOCol + cb * 32, o);
+            tmem_wait_ld();
+            if (takes) {
+              float *orow = a.ws_o + pr * D + cb * 32;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4 *>(orow + q * 4) =
+                    make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
+                                o[4 * q + 3] * inv);
+            }
+          }
+        } else {
+        T *orow = static_cast<T *>(a.out) + orow_idx * D;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           float o[32];
@@ -407,6 +517,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
               *reinterpret_cast<uint4 *>(orow + cb * 32 + q * 8) = pk;
             }
           }
+        }
         }
       } else if (lane == 0) {
         atomicOr(a.err, kErrTimeout);
@@ -504,7 +615,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     const int bs_mask = (1 << a.bs_log2) - 1;
     auto block_of = [&](int u) -> int {
       if (u >= n_sub) return -1;
-      const int phys = bt_row[(u * 16) >> a.bs_log2];
+      const int phys = table_entry(u);
       if (phys < 0 || static_cast<int64_t>(phys) >= a.num_blocks) {
         atomicOr(a.err, kErrBadBlock);
         return -1;
@@ -527,7 +638,8 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
         if (lane < kSub && my_phys >= 0) {
           const int u = n * kSub + lane;
-          const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((u * 16) & bs_mask);
+          const int y =
+              ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((key_base + u * 16) & bs_mask);
 #pragma unroll
           for (int b = 0; b < kAtoms; ++b)
             tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
@@ -622,15 +734,24 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   grid_launch_dependents();
 }
 
-template <typename T, int D, int SK, int SV, bool SPLIT, int TILES>
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX = false>
 cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km,
                                      const CUtensorMap &vm, cudaStream_t stream) {
-  constexpr size_t smem = PairLayout<SK, SV, TILES, D>::kSmem;
+  // the shared-prefix pass keeps each member's first partition and the pass's
+  // control words after the barriers
+  constexpr size_t smem = PairLayout<SK, SV, TILES, D>::kSmem + (PX ? (kTcRows + 8) * 4 : 0);
   static_assert(smem <= (TILES == 1 ? 113 : 227) * 1024, "shared memory");
-  auto kern = pa_prefill_tc_pair_kernel<T, D, SK, SV, SPLIT, TILES>;
+  auto kern = pa_prefill_tc_pair_kernel<T, D, SK, SV, SPLIT, TILES, PX>;
   static SmemLimitOnce smem_limit;
   const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
+  if constexpr (PX) {
+    return launch_dependent(
+        kern,
+        dim3(static_cast<unsigned>(a.num_parts * a.chunks), static_cast<unsigned>(a.num_kv_heads),
+             static_cast<unsigned>(a.num_groups)),
+        dim3(pair_threads<TILES>()), smem, stream, km, vm, a);
+  }
   const int tpc = TILES * kTcRows / a.group;
   const int tiles = (a.max_q_len + tpc - 1) / tpc;
   return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(pair_threads<TILES>()), smem,
@@ -695,6 +816,57 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void
   if (!prefill_tc_supported(head_dim, a.group)) return cudaErrorInvalidValue;
   return head_dim == 128 ? launch_prefill_tc_d<128>(a, km, vm, dtype, stream)
                          : launch_prefill_tc_d<64>(a, km, vm, dtype, stream);
+}
+
+// The shared-prefix pass of pa_decode_shared_prefix on the same kernel: one
+// 128-row tile per CTA (two CTAs per SM) holding the (member, query head) rows
+// of 128 / G members of a group, over one partition of the group's shared
+// prefix.
+int shared_prefix_members_per_cta(int group) { return kTcRows / group; }
+
+cudaError_t launch_shared_prefix(const DecodeArgs &d, const void *k_cache, const void *v_cache,
+                                 int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
+                                 bool *map_failed) {
+  CUtensorMap km, vm;
+  *map_failed = false;
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, false) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, false)) {
+    *map_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  PrefillArgs a{};
+  a.query = d.query;
+  a.block_tables = d.block_tables;
+  a.context_lens = d.context_lens;
+  a.max_blocks_per_seq = d.max_blocks_per_seq;
+  a.num_seqs = d.num_seqs;
+  a.num_q_heads = d.num_q_heads;
+  a.num_kv_heads = d.num_kv_heads;
+  a.group = d.group;
+  a.bs_log2 = d.bs_log2;
+  a.num_blocks = d.num_blocks;
+  a.scale_log2 = d.scale_log2;
+  a.err = d.err;
+  a.ws_m = d.ws_m;
+  a.ws_l = d.ws_l;
+  a.ws_o = d.ws_o;
+  a.prefix_lens = d.prefix_lens;
+  a.group_start = d.group_start;
+  a.num_groups = d.num_groups;
+  a.max_group_size = d.max_group_size;
+  a.members_per_cta = d.members_per_cta;
+  a.chunks = d.chunks;
+  a.part_tokens = d.part_tokens;
+  a.num_parts = d.num_parts;
+  a.max_context_len = d.max_context_len;
+  constexpr int KS = PA_PREFILL_SOLO_KSTAGES, VS = PA_PREFILL_SOLO_VSTAGES;
+  if (dtype == 0)
+    return head_dim == 128
+               ? launch_prefill_tc_pair_t<__half, 128, KS, VS, false, 1, true>(a, km, vm, stream)
+               : launch_prefill_tc_pair_t<__half, 64, KS, VS, false, 1, true>(a, km, vm, stream);
+  return head_dim == 128
+             ? launch_prefill_tc_pair_t<__nv_bfloat16, 128, KS, VS, true, 1, true>(a, km, vm, stream)
+             : launch_prefill_tc_pair_t<__nv_bfloat16, 64, KS, VS, true, 1, true>(a, km, vm, stream);
 }
 
 }  // namespace pa
