@@ -198,7 +198,7 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
  * RadixAttention; "Serving engines", How vLLM works).  The result is
  * pa_decode's for the same arguments (the same formula, within rounding);
  * the difference is the memory traffic: the K/V of a group's shared prefix
- * is read once per group (per 16 query heads of it) instead of once per
+ * is read once per group (per 128 query heads of it) instead of once per
  * sequence.
  *
  * group_start   device int32 [num_groups + 1]: group g is the sequences

@@ -118,24 +118,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
-// Four 8x8 b16 matrices from shared memory: lanes 8i .. 8i+7 give the row
-// addresses (16 bytes each) of matrix i; d[i] receives matrix i in the MMA
-// fragment layout (lane t: row t / 4, elements 2 (t % 4) and 2 (t % 4) + 1).
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&d)[4], const void *row) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-               : "r"(smem_addr(row))
-               : "memory");
-}
-// The same with each matrix transposed (lane t: column t / 4, rows 2 (t % 4)
-// and 2 (t % 4) + 1).
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&d)[4], const void *row) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-               : "r"(smem_addr(row))
-               : "memory");
-}
-
 // Element types: packing two fp32 values into one 32-bit register (low half =
 // first value, round to nearest even), unpacking, and the matching tensor-core MMA
 // D(16x8, fp32) += A(16x16) * B(16x8).

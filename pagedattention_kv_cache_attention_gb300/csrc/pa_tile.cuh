@@ -1,7 +1,6 @@
-// pa_tile.cuh -- the per-sub-tile arithmetic of paged decode attention over a
-// 16-bit KV cache, shared by the decode kernel (one sequence's query heads per
-// MMA column tile) and the shared-prefix kernel (the query heads of several
-// sequences per column tile).
+// pa_tile.cuh -- the per-sub-tile arithmetic of the paged decode kernel over
+// a 16-bit KV cache, and the sub-tile geometry and softmax step it shares with
+// the FP8 path.
 //
 // A sub-tile is 16 consecutive rows of one physical block, K or V, staged in
 // shared memory by 2-D TMA copies in 128-byte boxes of 16 rows with the
@@ -51,16 +50,6 @@ template <int D, bool F8> __device__ __forceinline__ int pv_dim_a(int g, int mt)
 }
 template <int D, bool F8> __device__ __forceinline__ int pv_dim_b(int g, int mt) {
   return F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
-}
-
-// The query fragment of column g (B operand of S^T = K Q^T) for a 16-bit
-// cache: chunks q_chunk(i, c) of the column's query row, zero for a padding
-// column (q == nullptr).
-template <typename MT, int D>
-__device__ __forceinline__ void load_q_16(const MT *q, int c, uint4 (&qf)[D / 32]) {
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i)
-    qf[i] = q ? *reinterpret_cast<const uint4 *>(q + q_chunk(i, c) * 8) : make_uint4(0, 0, 0, 0);
 }
 
 // S^T = K Q^T for one 16-bit sub-tile: sc[0..1] = tokens g (columns 2c, 2c+1),

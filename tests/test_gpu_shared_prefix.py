@@ -5,7 +5,7 @@ The oracle knows nothing of prefix groups: it attends every sequence over its
 own tokens through its own block table, exactly as for pa_decode.  The shared
 pass must therefore reproduce per-sequence attention while reading each group's
 shared prefix once.  Cases span several partitions, group chunks (groups with
-more than one CTA's 16 query rows), members shorter than the shared prefix,
+more than one CTA's 128 query rows), members shorter than the shared prefix,
 partitions joined inside the decode kernel and by the reduce kernel, and the
 device-side checks of the group description.
 """
@@ -103,15 +103,15 @@ class SharedRun:
 CASES = [
     (3, 2, 256, 40, 64, 32, 8, 128, 16, "fp16"),     # G 4, 4 shared partitions
     (2, 5, 300, 64, 64, 32, 8, 128, 16, "bf16"),     # prefix not a multiple of the partition
-    (1, 9, 128, 30, 32, 32, 8, 128, 16, "fp16"),     # 9 members at G 4: two CTA chunks
-    (2, 6, 192, 50, 64, 64, 8, 128, 32, "fp16"),     # G 8, bs 32: 4 members per chunk
+    (1, 37, 128, 30, 32, 32, 8, 128, 16, "fp16"),    # 37 members at G 4: two CTA chunks (32 + 5)
+    (2, 18, 192, 50, 64, 64, 8, 128, 32, "fp16"),    # G 8, bs 32: 16 members per chunk, two chunks
     (3, 4, 160, 20, 32, 8, 8, 64, 16, "bf16"),       # MHA (G 1), head_dim 64
     (2, 11, 96, 33, 32, 12, 4, 64, 32, "fp16"),      # G 3: columns cut across members
     (4, 3, 40, 16, 16, 32, 8, 128, 16, "fp16"),      # partial prefix block (copied, not shared)
     (2, 3, 64, 8, 64, 32, 8, 128, 16, "bf16"),       # prefix = one partition
     (5, 1, 128, 40, 32, 32, 8, 128, 16, "fp16"),     # groups of one
-    (2, 7, 144, 30, 48, 40, 8, 128, 16, "bf16"),     # G 5 (15 of 16 rows); 3 sub-tiles per partition
-    (3, 5, 112, 24, 16, 56, 8, 64, 32, "fp16"),      # G 7 (14 rows), one sub-tile per partition
+    (2, 27, 144, 30, 48, 40, 8, 128, 16, "bf16"),    # G 5 (125 of 128 rows, 25 + 2 members); 48-token partitions
+    (3, 5, 112, 24, 16, 56, 8, 64, 32, "fp16"),      # G 7 (35 of 128 rows), 16-token partitions
 ]
 
 
@@ -153,9 +153,9 @@ def test_many_partitions_join_in_the_reduce_kernel(pa):
 def test_loose_group_size_bound(pa):
     """max_group_size above every group's size: the extra chunks find no
     members and leave."""
-    w = W.make("shared_prefix_cow", seed=13, groups=3, group_size=3, prefix_len=128, max_len=40,
-               partition_size=32)
-    r = SharedRun(pa, w, 32, max_group_size=w.num_seqs)
+    w = W.make("shared_prefix_cow", seed=13, groups=4, group_size=5, prefix_len=128, max_len=40,
+               num_q_heads=64, num_kv_heads=8, partition_size=32)
+    r = SharedRun(pa, w, 32, max_group_size=w.num_seqs)   # 16 members per CTA: a second chunk
     assert r.err == 0
     r.check("loose group-size bound")
 

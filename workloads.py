@@ -19,7 +19,8 @@ Workloads (sizes as the decode batches they stand in for):
   tiny_mha           4 seqs, 4 q = 4 kv heads, d 64,  bs 16, ctx U[1,200], 64-block pool
   llama3_8b_gqa      64 seqs, 32 q / 8 kv heads, d 128, bs 16, ctx U[512,4096], pool +10%,
                      1024-token partitions
-  shared_prefix_cow  16 groups x 8 seqs sharing a 2048-token prefix, suffix U[1,512]
+  shared_prefix_cow  16 groups x 8 seqs sharing a 2048-token prefix, suffix U[1,512],
+                     1024-token partitions
   long_context       8 seqs, 32/8 heads, d 128, bs 16, ctx {32768 x6, 65536, 131072}, bf16
   llama3_70b_cb      256 seqs, 64/8 heads, d 128, bs 32, ctx lognormal(ln 1024, 1.0)
                      clipped to [1,16384], pool +20%, fp16 or bf16, 2048-token partitions
@@ -324,7 +325,7 @@ def make(name: str, seed: int = 0, *, dtype: Optional[str] = None, batch: Option
         grp = [list(range(g * gs, (g + 1) * gs)) for g in range(ng)]
         return _build(name, seed, dtype or "fp16", B, num_q_heads or 32, num_kv_heads or 8,
                       head_dim or 128, block_size or 16, ctx, 1.1,
-                      partition_size if partition_size is not None else 512, rng, gen,
+                      partition_size if partition_size is not None else 1024, rng, gen,
                       prefix_groups=grp, prefix_len=P, table_len=P + (max_len or 512))
     if name == "long_context":
         ctx = np.asarray(lens) if lens is not None else np.array([32768] * 6 + [65536, 131072])
