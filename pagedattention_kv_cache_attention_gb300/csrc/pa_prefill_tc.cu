@@ -1,13 +1,20 @@
 // pa_prefill_tc.cu -- chunked-prefill attention on the fifth-generation tensor
 // core (tcgen05: accumulators and P in tensor memory, operands staged by TMA).
 //
-// Same computation as pa_prefill.cu ("Serving engines", How vLLM works:
-// chunked prefill; chunk row t at position ctx - q_len + t attends causally to
-// tokens 0..t's position through the block table), for head_dim 64 or 128 and
-// every query group G from 1 to 8.  One kernel template, two shapes: two
-// 128-row query tiles per CTA (one CTA per SM) for chunks longer than 128/G
-// tokens, one tile per CTA (two CTAs per SM) for shorter ones.  The design and
-// the measurements that shaped it are described above the kernel.
+// Chunked prefill ("Serving engines", How vLLM works: chunked prefill; chunk
+// row t at position ctx - q_len + t attends causally to tokens 0..t's position
+// through the block table), for head_dim 64 or 128 and every query group G
+// from 1 to 8.  One kernel template, two shapes: two 128-row query tiles per
+// CTA (one CTA per SM) for chunks longer than 128/G tokens, one tile per CTA
+// (two CTAs per SM) for shorter ones.  The design and the measurements that
+// shaped it are described above the kernel.
+//
+// The same kernel, with its shared-prefix flag, is the shared pass of
+// pa_decode_shared_prefix: a tile's rows are then the (sequence, query head)
+// pairs of the members of a group of sequences that share a prefix in the same
+// physical blocks ("LLM Serving Engine Shootout", 3.2 Copy-on-Write), its keys
+// one partition of that prefix with no causal limit, and its rows leave split
+// partials (m, l, o) in the decode workspace for the decode kernel to join.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
