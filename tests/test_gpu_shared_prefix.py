@@ -179,11 +179,13 @@ def test_one_partition_is_plain_decode(pa):
     assert torch.equal(r.out, r.plain)
 
 
-def test_full_size_shared_prefix_batch(pa):
+@pytest.mark.parametrize("heads", [(32, 8), (64, 8)], ids=["G4", "G8"])
+def test_full_size_shared_prefix_batch(pa, heads):
     """The copy-on-write batch at full size (16 groups x 8 sequences, 2048-token
-    prefix, 512-token partitions): every sequence of a sample against the
-    oracle, and every output against pa_decode."""
-    w = W.make("shared_prefix_cow")
+    prefix, the batch's 1024-token partitions), with its own head shape and the
+    70B one: every sequence of a sample against the oracle, and every output
+    against pa_decode."""
+    w = W.make("shared_prefix_cow", num_q_heads=heads[0], num_kv_heads=heads[1])
     r = SharedRun(pa, w, w.partition_size)
     assert r.err == 0
     rng = np.random.default_rng(0)
