@@ -303,7 +303,7 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
  * (dtype = PA_FP16) or bf16 (PA_BF16): bf16 queries are scaled by a power of
  * two per (sequence, KV head) so that their largest magnitude fits fp16, then
  * rounded to fp16 (exact for every value down to 2^-31 of the largest), and
- * the power of two is taken back out of the softmax scale.  head_dim 128,
+ * the power of two is taken back out of the softmax scale.  head_dim 64 or 128,
  * block_size 16 or 32.  Workspace as for pa_decode.
  */
 pa_status pa_decode_fp8(void *out, const void *query,

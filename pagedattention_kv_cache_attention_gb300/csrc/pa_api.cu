@@ -370,7 +370,6 @@ pa_status pa_decode_fp8(void *out, const void *query, const void *k_cache, const
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
       !(v_scale > 0.f) || dtype != PA_FP16 && dtype != PA_BF16)
     return PA_ERR_INVALID_ARG;
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   return decode_impl(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, max_context_len, partition_size, workspace,

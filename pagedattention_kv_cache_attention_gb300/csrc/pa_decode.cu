@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(NW * 32)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<D, F8>;
-  static_assert(!F8 || (D == 128 && sizeof(T) == 2), "FP8 caches: head_dim 128, 16-bit queries");
+  static_assert(!F8 || sizeof(T) == 2, "FP8 caches: 16-bit queries");
   // MMA operand type: the query type, except over FP8 caches, whose codes are
   // exact in fp16 (and not all in bf16's exponent range with fp16's
   // precision): there the queries are carried in fp16 (see the q load)
@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(NW * 32)
                     (static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + g) * D;
 #pragma unroll
     for (int i = 0; i < Sh::kQChunks; ++i) {
-      const int ch = F8 ? 2 * (2 * c + (i >> 1)) + (i & 1) : q_chunk(i, c);
+      // FP8: lane c reads 16-dim units c D/64 + j of each K row (j < D/64)
+      const int ch = F8 ? 2 * (c * (D / 64) + (i >> 1)) + (i & 1) : q_chunk(i, c);
       qf[i] = g < G ? *reinterpret_cast<const uint4 *>(qrow + ch * 8) : make_uint4(0, 0, 0, 0);
     }
     if constexpr (F8 && !std::is_same<T, __half>::value) {
@@ -372,13 +373,15 @@ __global__ void __launch_bounds__(NW * 32)
         qk_subtile_16<MT, D>(Ks, qf, g, c, sc[h]);
       } else {
         sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
-        // unit 2c + j of rows g and g+8 holds 16 dims: four k16 steps
+        // unit c D/64 + j of rows g and g+8 holds 16 dims: four k16 steps
+        // (rows g and g+8 share their swizzle, so each quarter-warp hits 8
+        // distinct 16-byte units of one 128-byte span)
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
-          const int sw = ((2 * c + j) ^ g) << 4;
+          const int u = c * (D / 64) + j;
           uint32_t ka[8], kb[8];
-          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + g * 128 + sw), ka);
-          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(Ks + (g + 8) * 128 + sw), kb);
+          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(f8_unit<D>(Ks, g, u)), ka);
+          e4m3x16_to_half(*reinterpret_cast<const uint4 *>(f8_unit<D>(Ks, g + 8, u)), kb);
           const uint32_t q[8] = {qf[2 * j].x, qf[2 * j].y, qf[2 * j].z, qf[2 * j].w,
                                  qf[2 * j + 1].x, qf[2 * j + 1].y, qf[2 * j + 1].z,
                                  qf[2 * j + 1].w};
@@ -406,22 +409,32 @@ __global__ void __launch_bounds__(NW * 32)
       if constexpr (!F8) {
         pv_subtile_16<MT, D>(Vs, nvalid[h], g, c, pb0, pb1, pr0, pr1, acc);
       } else {
-        // unit g (dims 16g .. 16g+15) of each row, still E4M3
+        // MMA row g of m-tile mt is dim dA = pv_dim_a(g, mt), row g+8 is dB:
+        // at head_dim 128 the 16 dims 16g .. 16g+15 (unit g of each row), at
+        // 64 the 8 dims 8g .. 8g+7 (half g % 2 of unit g / 2); each byte
+        // interleave of two rows yields the (token 2c, token 2c+1) pairs of
+        // two m-tiles, still E4M3
+        constexpr int kHi = D == 128 ? 8 : 4;  // byte of dB within the lane's dims
         uint4 v8[4];
 #pragma unroll
         for (int ri = 0; ri < 4; ++ri) {
           const int r = 2 * c + (ri & 1) + 8 * (ri >> 1);
-          const uint4 xv = *reinterpret_cast<const uint4 *>(Vs + r * 128 + ((g ^ (r & 7)) << 4));
+          uint4 xv;
+          if constexpr (D == 128) {
+            xv = *reinterpret_cast<const uint4 *>(f8_unit<D>(Vs, r, g));
+          } else {
+            const uint2 half_unit =
+                *reinterpret_cast<const uint2 *>(f8_unit<D>(Vs, r, g >> 1) + (g & 1) * 8);
+            xv = make_uint4(half_unit.x, half_unit.y, 0u, 0u);
+          }
           v8[ri] = r < nvalid[h] ? xv : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int mt = 0; mt < Sh::kMTiles; mt += 2) {
-          // MMA row g is dim 16g + mt, row g+8 is dim 16g + 8 + mt; each byte
-          // interleave yields the (token 2c, token 2c+1) pairs of two m-tiles
           const uint32_t w0 = interleave_bytes(v8[0], v8[1], mt);
-          const uint32_t w1 = interleave_bytes(v8[0], v8[1], 8 + mt);
+          const uint32_t w1 = interleave_bytes(v8[0], v8[1], kHi + mt);
           const uint32_t w2 = interleave_bytes(v8[2], v8[3], mt);
-          const uint32_t w3 = interleave_bytes(v8[2], v8[3], 8 + mt);
+          const uint32_t w3 = interleave_bytes(v8[2], v8[3], kHi + mt);
           {
             const uint32_t a0 = e4m3x2_lo_to_f16x2(w0), a1 = e4m3x2_lo_to_f16x2(w1);
             const uint32_t a2 = e4m3x2_lo_to_f16x2(w2), a3 = e4m3x2_lo_to_f16x2(w3);
@@ -733,21 +746,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }  // namespace
 
 // The pool viewed as a 2-D tensor [num_blocks * num_kv_heads * block_size rows,
-// head_dim] loaded in boxes of 16 rows x 128 bytes with the 128-byte swizzle.
+// head_dim] loaded in boxes of 16 rows x 128 bytes with the 128-byte swizzle
+// (rows of 64 bytes -- an FP8 cache at head_dim 64 -- in 64-byte boxes with
+// the 64-byte swizzle).
 bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int dtype,
                      bool fp8) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int elem = fp8 ? 1 : 2;
+  const int box_row = head_dim * elem < 128 ? head_dim * elem : 128;  // bytes
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elem};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_row / elem), static_cast<cuuint32_t>(kTile)};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                      : (dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUresult r = enc(map, ty, 2, const_cast<void *>(pool), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   box_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -830,11 +847,17 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
     *map_failed = true;
     return cudaErrorInvalidValue;
   }
-  if (kv_fp8)
+  if (kv_fp8) {
+    if (head_dim == 128)
+      return dtype == 0
+                 ? launch_decode_t<__half, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream)
+                 : launch_decode_t<__nv_bfloat16, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
+                                                                                         stream);
     return dtype == 0
-               ? launch_decode_t<__half, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream)
-               : launch_decode_t<__nv_bfloat16, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
-                                                                                       stream);
+               ? launch_decode_t<__half, 64, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream)
+               : launch_decode_t<__nv_bfloat16, 64, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
+                                                                                      stream);
+  }
   if (dtype == 0) {
     return head_dim == 128
                ? launch_decode_t<__half, 128, kWarps, kStages, false, kNsub>(a, km, vm, stream)

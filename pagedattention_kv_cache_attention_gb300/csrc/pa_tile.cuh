@@ -25,17 +25,28 @@ namespace pa {
 constexpr int kTile = 16;  // tokens per sub-tile (one MMA row block)
 constexpr unsigned kFull = 0xffffffffu;
 
-// Geometry of one sub-tile in shared memory.
+// Geometry of one sub-tile in shared memory.  Rows of 128 bytes or more are
+// staged in 128-byte box rows with the 128-byte swizzle; the 64-byte rows of
+// an FP8 cache at head_dim 64 in 64-byte box rows with the 64-byte swizzle
+// (16-byte unit u of row r at unit u ^ ((r >> 1) & 3)).
 template <int D, bool F8> struct Shape {
   static constexpr int kElem = F8 ? 1 : 2;               // bytes per cached element
   static constexpr int kRowBytes = D * kElem;
-  static constexpr int kBoxElems = 128 / kElem;          // elements per 128-byte box row
-  static constexpr int kBoxes = kRowBytes / 128;         // boxes per row
-  static constexpr int kBoxBytes = kTile * 128;          // one box of 16 rows
+  static constexpr int kBoxRow = kRowBytes < 128 ? kRowBytes : 128;  // bytes per box row
+  static constexpr int kBoxElems = kBoxRow / kElem;      // elements per box row
+  static constexpr int kBoxes = kRowBytes / kBoxRow;     // boxes per row
+  static constexpr int kBoxBytes = kTile * kBoxRow;      // one box of 16 rows
   static constexpr int kTileBytes = kTile * kRowBytes;   // K (or V) of one sub-tile
   static constexpr int kQChunks = D / 32;                // 16-byte q chunks per lane
   static constexpr int kMTiles = D / 16;                 // m16 tiles of the P.V product
 };
+
+// Address of 16-byte unit u of row r of an FP8 sub-tile (one box per row).
+template <int D>
+__device__ __forceinline__ const uint8_t *f8_unit(const uint8_t *tile, int r, int u) {
+  return D == 128 ? tile + r * 128 + ((u ^ (r & 7)) << 4)
+                  : tile + r * 64 + ((u ^ ((r >> 1) & 3)) << 4);
+}
 
 // 16-bit caches: the 16-byte chunk (8 elements) of a head_dim row that lane
 // column c reads in QK^T step i.  Every chunk is read by exactly one (i, c);
@@ -46,10 +57,10 @@ __device__ __forceinline__ int q_chunk(int i, int c) { return 2 * c + (i & 1) + 
 // Output dimensions of P.V m-tile mt held by lane row g: row g of the MMA is
 // dimension dA, row g + 8 is dB.
 template <int D, bool F8> __device__ __forceinline__ int pv_dim_a(int g, int mt) {
-  return F8 ? 16 * g + mt : 8 * g + mt;
+  return F8 && D == 128 ? 16 * g + mt : 8 * g + mt;
 }
 template <int D, bool F8> __device__ __forceinline__ int pv_dim_b(int g, int mt) {
-  return F8 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
+  return F8 && D == 128 ? 16 * g + 8 + mt : (D == 128 ? 64 + 8 * g + mt : 8 * g + 4 + mt);
 }
 
 // S^T = K Q^T for one 16-bit sub-tile: sc[0..1] = tokens g (columns 2c, 2c+1),

@@ -73,7 +73,12 @@ CASES = [("llama3_8b_gqa", dict(lens=[1, 15, 16, 17, 100, 513, 2049], num_q_head
          ("llama3_70b_cb", dict(lens=[1, 31, 32, 33, 700, 3000], dtype="bf16")),
          ("long_context", dict(lens=[9000, 3])),
          ("llama3_8b_gqa", dict(lens=[5, 600], num_q_heads=24, num_kv_heads=8, block_size=32,
-                                dtype="bf16"))]
+                                dtype="bf16")),
+         # head_dim 64: 64-byte rows, staged with the 64-byte swizzle
+         ("tiny_mha", dict(lens=[1, 15, 16, 17, 100, 200])),
+         ("llama3_8b_gqa", dict(lens=[1, 33, 700, 2049], head_dim=64)),
+         ("llama3_8b_gqa", dict(lens=[5, 600, 1500], head_dim=64, num_q_heads=64, num_kv_heads=8,
+                                block_size=32, dtype="bf16"))]
 
 
 @pytest.mark.parametrize("name,kw", CASES, ids=[f"{n}-{i}" for i, (n, _) in enumerate(CASES)])
@@ -102,12 +107,14 @@ def test_fp8_full_size(pa, name, dtype):
 @pytest.mark.parametrize("i", range(12))
 def test_fp8_random_shapes(pa, i):
     """Seeded random FP8 decode shapes: batch 1-8, contexts 0-3000, group 1-8,
-    1-8 KV heads, block size 16 or 32, one partition size each."""
+    1-8 KV heads, head_dim 64 or 128, block size 16 or 32, one partition size
+    each."""
     rng = np.random.default_rng(4000 + i)
     G, hkv = int(rng.integers(1, 9)), int(rng.choice([1, 2, 4, 8]))
     lens = [int(x) for x in rng.integers(0, 3001, int(rng.integers(1, 9)))]
     w = W.to_fp8(W.make("llama3_8b_gqa", 120 + i, lens=lens, num_q_heads=G * hkv,
                         num_kv_heads=hkv, block_size=int(rng.choice([16, 32])),
+                        head_dim=int(rng.choice([64, 128])),
                         dtype=str(rng.choice(["fp16", "bf16"]))))
     ps = int(rng.choice([0, 16, 48, 160, 512]))
     kc, vc, outs = run_fp8(pa, w, [ps])
@@ -158,16 +165,3 @@ def test_fp8_permutation_bitwise(pa):
     _, _, b = run_fp8(pa, w.permuted(3), [0, 1024])
     for ps in (0, 1024):
         assert torch.equal(a[ps].view(torch.int16), b[ps].view(torch.int16))
-
-
-def test_fp8_unsupported_shapes(pa):
-    import ctypes
-    w = W.make("tiny_mha", 44)   # head_dim 64
-    f8 = W.to_fp8(w)
-    dev = torch.device("cuda")
-    q = w.query.to(dev)
-    with pytest.raises(pa.PaError) as e:
-        pa.pa_decode_fp8(torch.empty_like(q), q, f8.k_cache.to(dev), f8.v_cache.to(dev),
-                         w.block_tables.to(dev), w.context_lens.to(dev), w.scale, 1.0, 1.0,
-                         w.max_context_len, 0)
-    assert e.value.status == 2
