@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(NW * 32)
   // exact in fp16 (and not all in bf16's exponent range with fp16's
   // precision): there the queries are carried in fp16 (see the q load)
   using MT = typename std::conditional<F8, __half, T>::type;
-  static_assert(NSUB == 1 || NSUB == 2, "one or two sub-tiles per step");
+  // (a step's sub-tiles never straddle a 32-entry block-id window)
+  static_assert(NSUB == 1 || NSUB == 2 || NSUB == 4, "1, 2 or 4 sub-tiles per step");
   static_assert(S * NSUB <= 16, "stage bits");
   constexpr int kStepBytes = 2 * NSUB * Sh::kTileBytes;  // K and V of one step
   extern __shared__ uint8_t smem_raw[];
@@ -833,9 +834,18 @@ constexpr int kStages = PA_DECODE_STAGES;
 #ifndef PA_DECODE_STAGES_F8
 #define PA_DECODE_STAGES_F8 2
 #endif
+// head_dim 64: half the bytes per sub-tile, so more sub-tiles share a step
+#ifndef PA_DECODE_NSUB_D64
+#define PA_DECODE_NSUB_D64 2
+#endif
+#ifndef PA_DECODE_NSUB_F8_D64
+#define PA_DECODE_NSUB_F8_D64 2
+#endif
 constexpr int kNsub = PA_DECODE_NSUB;
 constexpr int kNsubF8 = PA_DECODE_NSUB_F8;
 constexpr int kStagesF8 = PA_DECODE_STAGES_F8;
+constexpr int kNsubD64 = PA_DECODE_NSUB_D64;
+constexpr int kNsubF8D64 = PA_DECODE_NSUB_F8_D64;
 
 cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *v_cache,
                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
@@ -854,20 +864,20 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
                  : launch_decode_t<__nv_bfloat16, 128, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
                                                                                          stream);
     return dtype == 0
-               ? launch_decode_t<__half, 64, kWarps, kStagesF8, true, kNsubF8>(a, km, vm, stream)
-               : launch_decode_t<__nv_bfloat16, 64, kWarps, kStagesF8, true, kNsubF8>(a, km, vm,
-                                                                                      stream);
+               ? launch_decode_t<__half, 64, kWarps, kStagesF8, true, kNsubF8D64>(a, km, vm, stream)
+               : launch_decode_t<__nv_bfloat16, 64, kWarps, kStagesF8, true, kNsubF8D64>(a, km, vm,
+                                                                                         stream);
   }
   if (dtype == 0) {
     return head_dim == 128
                ? launch_decode_t<__half, 128, kWarps, kStages, false, kNsub>(a, km, vm, stream)
-               : launch_decode_t<__half, 64, kWarps, kStages, false, kNsub>(a, km, vm, stream);
+               : launch_decode_t<__half, 64, kWarps, kStages, false, kNsubD64>(a, km, vm, stream);
   }
   return head_dim == 128
              ? launch_decode_t<__nv_bfloat16, 128, kWarps, kStages, false, kNsub>(a, km, vm,
                                                                                    stream)
-             : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages, false, kNsub>(a, km, vm,
-                                                                                 stream);
+             : launch_decode_t<__nv_bfloat16, 64, kWarps, kStages, false, kNsubD64>(a, km, vm,
+                                                                                    stream);
 }
 
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream) {
