@@ -137,6 +137,66 @@ __device__ __forceinline__ void join_partitions(const DecodeArgs &a, int seq, in
   }
 }
 
+// The same join, by a CTA that holds one partition of the row itself: its
+// unnormalised (M, L, o) of output elements 8 ch .. 8 ch + 7 are folded with
+// the partials of partitions [0, np) (written by another grid, complete by
+// now), and o leaves normalised.
+template <int D>
+__device__ __forceinline__ void join_into(const DecodeArgs &a, int64_t row, int ch, int np,
+                                          float M, float L, float (&o)[8]) {
+  constexpr int kGroup = 4;
+  const float *mrow = a.ws_m + row * a.num_parts;
+  const float *lrow = a.ws_l + row * a.num_parts;
+  const float *orow = a.ws_o + row * a.num_parts * D + ch * 8;
+  float W = L;  // the own partition's weight; L o_norm = o out_scale
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] *= a.out_scale;
+  for (int p0 = 0; p0 < np; p0 += kGroup) {
+    float mp[kGroup], lp[kGroup];
+    float4 oa[kGroup], ob[kGroup];
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      if (p0 + u < np) {
+        mp[u] = __ldcg(mrow + p0 + u);
+        lp[u] = __ldcg(lrow + p0 + u);
+        const float4 *src =
+            reinterpret_cast<const float4 *>(orow + static_cast<int64_t>(p0 + u) * D);
+        oa[u] = __ldcg(src);
+        ob[u] = __ldcg(src + 1);
+      } else {
+        mp[u] = -INFINITY;
+        lp[u] = 0.f;
+        oa[u] = ob[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) Mn = fmaxf(Mn, mp[u]);
+    const float ref = Mn == -INFINITY ? 0.f : Mn;  // no token yet: any finite reference
+    const float al = exp2f(M - ref);
+    W *= al;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] *= al;
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const float wgt = lp[u] * exp2f(mp[u] - ref);
+      W += wgt;
+      o[0] += wgt * oa[u].x;
+      o[1] += wgt * oa[u].y;
+      o[2] += wgt * oa[u].z;
+      o[3] += wgt * oa[u].w;
+      o[4] += wgt * ob[u].x;
+      o[5] += wgt * ob[u].y;
+      o[6] += wgt * ob[u].z;
+      o[7] += wgt * ob[u].w;
+    }
+    M = Mn;
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] *= inv;
+}
+
 // T: query/output type (and the MMA type); F8: the caches hold FP8 E4M3 codes
 // (T is then fp16), converted exactly to fp16 in registers.  NSUB: 16-token
 // sub-tiles per pipeline step (their MMA chains are independent and share one
@@ -538,6 +598,10 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncthreads();
 
+  // A shared-prefix sequence whose partitions but this one all come from the
+  // shared-prefix grid (complete since the wait above): this CTA joins them
+  // at once, from its own merge, with no counter and no partial of its own.
+  const bool join_here = a.fuse_join && first > 0 && np_seq - first == 1;
   constexpr int kChunks = D / 8;
   for (int item = threadIdx.x; item < G * kChunks; item += NW * 32) {
     const int h = item / kChunks, ch = item % kChunks;
@@ -554,11 +618,15 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] += src[e] * f;
     }
-    const float inv = L > 0.f ? a.out_scale / L : 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] *= inv;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h;
-    if (a.num_parts == 1 || (a.fuse_join && np_seq == 1)) {
+    if (join_here) {
+      join_into<D>(a, row, ch, first, M, L, o);
+    } else {
+      const float inv = L > 0.f ? a.out_scale / L : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] *= inv;
+    }
+    if (a.num_parts == 1 || (a.fuse_join && np_seq == 1) || join_here) {
       uint4 pk;
       pk.x = Elem<T>::pack(o[0], o[1]);
       pk.y = Elem<T>::pack(o[2], o[3]);
@@ -576,7 +644,7 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
-  if (a.fuse_join && np_seq > 1) {
+  if (a.fuse_join && np_seq > 1 && !join_here) {
     // count this partition in; the CTA that completes the count joins them
     // all (with a shared prefix, the partials of partitions below `first`
     // come from the shared-prefix grid, which finished before this one began).  The barrier orders every thread's partial stores before thread 0's
