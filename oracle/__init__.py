@@ -70,7 +70,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.pa_oracle_lse_combine.restype = None
     L.pa_oracle_max_threads.restype = i32
     L.pa_oracle_prefill.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64,
-                                    ctypes.c_float, i32, i32]
+                                    ctypes.c_float, i32, i32, ctypes.c_double, ctypes.c_double,
+                                    i32]
     L.pa_oracle_prefill.restype = i32
     return L
 
@@ -197,13 +198,17 @@ def decode(query, k_cache, v_cache, block_tables, context_lens, scale: float, dt
 
 
 def prefill(query, query_start, k_cache, v_cache, block_tables, context_lens, scale: float,
-            dtype: str, threads: int = 0) -> np.ndarray:
+            dtype: str, threads: int = 0, kv_dtype: str = None, k_scale: float = 1.0,
+            v_scale: float = 1.0) -> np.ndarray:
     """fp64 causal attention of each chunk row (position ctx - q_len + t) over
-    tokens 0 .. its position.  query [total_q, Hq, d]; returns the same shape."""
+    tokens 0 .. its position.  query [total_q, Hq, d]; returns the same shape.
+    ``kv_dtype`` "e4m3" reads uint8 caches whose codes stand for k_scale*e /
+    v_scale*e, as in ``decode``."""
+    kv_dtype = kv_dtype or dtype
     q = _u16(query)
     qs = _i32(query_start)
-    kc = _u16(k_cache)
-    vc = _u16(v_cache)
+    kc = _kv(k_cache, kv_dtype)
+    vc = _kv(v_cache, kv_dtype)
     bt = _i32(block_tables)
     cl = _i32(context_lens)
     total_q, Hq, d = q.shape
@@ -212,7 +217,8 @@ def prefill(query, query_start, k_cache, v_cache, block_tables, context_lens, sc
     assert qs.shape[0] == B + 1 and int(qs[-1]) == total_q
     out = np.empty((total_q, Hq, d), dtype=np.float64)
     rc = lib().pa_oracle_prefill(_p(out), _p(q), _p(qs), _p(kc), _p(vc), _p(bt), bt.shape[1],
-                                 _p(cl), B, Hq, Hkv, d, bs, NB, float(scale), DT[dtype], threads)
+                                 _p(cl), B, Hq, Hkv, d, bs, NB, float(scale), DT[dtype],
+                                 DT[kv_dtype], float(k_scale), float(v_scale), threads)
     if rc:
         raise IndexError(f"oracle prefill: status {rc}")
     return out

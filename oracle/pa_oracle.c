@@ -412,12 +412,15 @@ int pa_oracle_decode(double *out, double *part_m, double *part_l, double *part_o
  * p = ctx_i - q_len_i + t and attends causally to tokens 0 .. p:
  *   out[row, h, :] = softmax_j(scale q[row, h] . K_j) V_j over j <= p.
  * query/out [total_q, Hq, d].  Rows are independent; each is the decode
- * computation on the sequence cut after position p.
+ * computation on the sequence cut after position p.  The caches are read as
+ * in pa_oracle_decode: kv_dtype E4M3 means codes standing for k_scale * e and
+ * v_scale * e, any other kv_dtype the query's 16-bit type (scales 1).
  */
 int pa_oracle_prefill(double *out, const uint16_t *query, const int32_t *query_start,
                       const void *k_cache, const void *v_cache, const int32_t *block_tables,
                       int MB, const int32_t *context_lens, int B, int Hq, int Hkv, int d, int bs,
-                      int64_t NB, float scale, int dtype, int nthreads)
+                      int64_t NB, float scale, int dtype, int kv_dtype, double k_scale,
+                      double v_scale, int nthreads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || bs <= 0)
         return ORC_BAD_ARG;
@@ -454,9 +457,11 @@ int pa_oracle_prefill(double *out, const uint16_t *query, const int32_t *query_s
         int rc = (K && V && q && s) ? ORC_OK : ORC_NO_MEM;
         const int32_t *bt_row = block_tables + (int64_t)i * MB;
         if (rc == ORC_OK)
-            rc = pa_oracle_gather(K, k_cache, dtype, 1.0, bt_row, MB, n, Hkv, h / group, d, bs, NB);
+            rc = pa_oracle_gather(K, k_cache, kv_dtype, k_scale, bt_row, MB, n, Hkv, h / group, d,
+                                  bs, NB);
         if (rc == ORC_OK)
-            rc = pa_oracle_gather(V, v_cache, dtype, 1.0, bt_row, MB, n, Hkv, h / group, d, bs, NB);
+            rc = pa_oracle_gather(V, v_cache, kv_dtype, v_scale, bt_row, MB, n, Hkv, h / group, d,
+                                  bs, NB);
         if (rc == ORC_OK) {
             const uint16_t *qrow = query + ((int64_t)row * Hq + h) * d;
             for (int c = 0; c < d; ++c)

@@ -579,6 +579,55 @@ def pin_prefill_chunks_compose():
         assert np.array_equal(two, one[rows])
 
 
+def _prefill_pool_fp8(pw):
+    kh, vh = pw.k_cache.numpy().copy(), pw.v_cache.numpy().copy()
+    oracle.reshape_and_cache_fp8(pw.key, pw.value, kh, vh, pw.slot_mapping, pw.dtype,
+                                 pw.k_scale, pw.v_scale)
+    return kh, vh
+
+
+def pin_prefill_fp8_single_token_is_decode():
+    """FP8 caches: a chunk of one token is an FP8 decode step (bit-identical)."""
+    pw = W.to_fp8(W.make_prefill("llama3_8b_gqa", 24, lens=[5, 17, 40, 333], num_q_heads=8,
+                                 num_kv_heads=2, q_lens=[1, 1, 1, 1], dtype="bf16"))
+    kh, vh = _prefill_pool_fp8(pw)
+    fp8 = dict(kv_dtype="e4m3", k_scale=pw.k_scale, v_scale=pw.v_scale)
+    got = oracle.prefill(pw.query, pw.query_start, kh, vh, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype, **fp8)
+    ref = oracle.decode(pw.query, kh, vh, pw.block_tables, pw.context_lens, pw.scale, pw.dtype,
+                        **fp8)
+    assert np.array_equal(got, ref)
+
+
+def pin_prefill_fp8_vs_torch_dequantised_sdpa():
+    """FP8 caches: whole-prompt prefill against torch's fp64 causal SDPA over
+    contiguous K/V whose codes are decoded by torch's own float8_e4m3fn type
+    and multiplied by the scales (not the oracle's decoder)."""
+    F = torch.nn.functional
+    ks, vs = 0.037, 0.11
+    pw = W.to_fp8(W.make_prefill("llama3_70b_cb", 25, lens=[50, 33], head_dim=64, num_q_heads=8,
+                                 num_kv_heads=2, chunk=10**6), k_scale=ks, v_scale=vs)
+    kh, vh = _prefill_pool_fp8(pw)
+    got = oracle.prefill(pw.query, pw.query_start, kh, vh, pw.block_tables, pw.context_lens,
+                         pw.scale, pw.dtype, kv_dtype="e4m3", k_scale=ks, v_scale=vs)
+    G, bs = 4, pw.block_size
+    for i in range(pw.num_seqs):
+        c = int(pw.context_lens[i])
+        bt = pw.block_tables[i].numpy()
+        idx = [(int(bt[j // bs]), j % bs) for j in range(c)]
+
+        def contiguous(cache, scale):
+            codes = np.stack([np.stack([cache[b, h, o] for b, o in idx]) for h in range(2)])
+            vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double() * scale
+            return vals.repeat_interleave(G, 0)
+        K, V = contiguous(kh, ks), contiguous(vh, vs)
+        q0 = int(pw.query_start[i])
+        Q = pw.query[q0:q0 + c].double().permute(1, 0, 2)
+        ref = F.scaled_dot_product_attention(Q[None], K[None], V[None], is_causal=True,
+                                             scale=float(np.float32(pw.scale)))[0]
+        assert np.allclose(got[q0:q0 + c], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+
+
 def pin_random_shapes_vs_brute_force():
     """Seeded sweep of small random shapes (group 1-8, 1/2/4 KV heads, head_dim
     64/128, block size 16/32, fp16/bf16, contexts 0-300): the oracle's decode
