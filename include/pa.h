@@ -318,6 +318,48 @@ pa_status pa_decode_fp8(void *out, const void *query,
                         int32_t dtype, void *stream);
 
 /*
+ * pa_prefill_fp8 -- pa_prefill over FP8 caches, K_j and V_j as in
+ * pa_decode_fp8.  The tcgen05 kernel copies each step's codes into shared
+ * memory and widens them there to fp16 (exact), so both products run in fp16
+ * with fp32 accumulation; k_scale joins the softmax scale and v_scale
+ * multiplies the output.  bf16 queries (dtype = PA_BF16) are scaled by a
+ * power of two per row (token, head) so that the row's largest magnitude
+ * fits fp16, rounded to fp16 (exact for every value down to 2^-31 of the
+ * largest), and the power of two is taken back out of that row's softmax
+ * scale; out is written in dtype.  k_scale, v_scale finite and > 0.  Other
+ * arguments, shapes and error behaviour as pa_prefill.
+ */
+pa_status pa_prefill_fp8(void *out, const void *query, const int32_t *query_start,
+                         const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, float scale,
+                         float k_scale, float v_scale, int32_t dtype, void *stream);
+
+/*
+ * pa_decode_shared_prefix_fp8 -- pa_decode_shared_prefix over FP8 caches: the
+ * result is pa_decode_fp8's for the same arguments (K_j, V_j, scales and
+ * queries as there); the shared pass reads the codes of a group's shared
+ * prefix once per group (per 128 query heads of it) and widens them as
+ * pa_prefill_fp8 does.  Group arguments, workspace and device checks as
+ * pa_decode_shared_prefix.
+ */
+pa_status pa_decode_shared_prefix_fp8(void *out, const void *query,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens,
+                                      const int32_t *group_start, const int32_t *prefix_lens,
+                                      int32_t num_groups, int32_t max_group_size,
+                                      int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks, float scale,
+                                      float k_scale, float v_scale,
+                                      int32_t max_context_len, int32_t partition_size,
+                                      void *workspace, size_t workspace_bytes,
+                                      int32_t dtype, void *stream);
+
+/*
  * pa_copy_blocks -- copy-on-write fork of whole physical blocks ("Serving
  * engines", How vLLM works: sequences share physical blocks until one writes;
  * the write forks only the block being written).
@@ -332,11 +374,16 @@ pa_status pa_decode_fp8(void *out, const void *query,
  *                   (otherwise the result is undefined).  A pair with an id
  *                   outside [0, num_blocks) is skipped and sets
  *                   PA_DEVERR_BAD_BLOCK.
- * head_dim in {64, 128}, block_size in {16, 32}.
+ * head_dim in {64, 128}, block_size in {16, 32}.  16-bit caches (fp16 or
+ * bf16, 2 bytes per element); pa_copy_blocks_fp8 is the same over FP8 caches
+ * (1 byte per element).
  */
 pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                          int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, int64_t num_blocks, void *stream);
+pa_status pa_copy_blocks_fp8(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                             int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int64_t num_blocks, void *stream);
 
 /*
  * pa_swap_blocks -- move whole blocks between two pools, typically the device
@@ -421,8 +468,9 @@ pa_status pa_selftest_bounded_wait(void *stream);
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(int32_t status);
 
-/* Library ABI version: 3 (2 added the join counters to the workspace, 3
-   pa_decode_shared_prefix). */
+/* Library ABI version: 4 (2 added the join counters to the workspace, 3
+   pa_decode_shared_prefix, 4 the FP8 forms of pa_prefill,
+   pa_decode_shared_prefix and pa_copy_blocks). */
 int32_t pa_version(void);
 
 #ifdef __cplusplus

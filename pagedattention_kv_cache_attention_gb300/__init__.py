@@ -27,7 +27,8 @@ __all__ = [
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_prefill", "pa_selftest_bounded_wait",
     "PaError", "DEVERR_BAD_BLOCK", "DEVERR_BAD_SLOT", "DEVERR_BAD_LEN", "DEVERR_TIMEOUT",
     "DEVERR_WORKSPACE", "DEVERR_PREFIX", "DECODE_COUNTER_BYTES", "new_decode_workspace",
-    "pa_decode_shared_prefix",
+    "pa_decode_shared_prefix", "pa_decode_shared_prefix_fp8", "pa_prefill_fp8",
+    "pa_copy_blocks_fp8",
 ]
 
 PA_FP16, PA_BF16 = 0, 1
@@ -203,29 +204,19 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
     return out
 
 
-def pa_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
-                            v_cache: torch.Tensor, block_tables: torch.Tensor,
-                            context_lens: torch.Tensor, group_start: torch.Tensor,
-                            prefix_lens: torch.Tensor, max_group_size: int, scale: float,
-                            max_context_len: int, partition_size: int,
-                            workspace: Optional[torch.Tensor] = None,
-                            stream=None) -> torch.Tensor:
-    """pa_decode over groups of sequences sharing a prefix in the same
-    physical blocks: ``group_start`` (int32 [num_groups + 1], runs of
-    consecutive sequences covering the batch) and ``prefix_lens`` (int32 [B],
-    shared leading tokens of each sequence, equal within a group) on the
-    device; ``max_group_size`` bounds the groups' sizes.  The shared prefix's
-    K/V is read once per group.  ``workspace`` as for pa_decode."""
-    L = _load()
-    if not getattr(L.pa_decode_shared_prefix, "argtypes", None):
-        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-        L.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32,
-                                              i32, i32, i32, i64, ctypes.c_float, i32, i32, P,
-                                              ctypes.c_size_t, i32, P]
-        L.pa_decode_shared_prefix.restype = i32
-    dt = k_cache.dtype
-    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
-        _cuda(n, t, dt)
+def _shared_prefix(name, out, query, k_cache, v_cache, block_tables, context_lens, group_start,
+                   prefix_lens, max_group_size, scale, scales, max_context_len, partition_size,
+                   workspace, stream):
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    fp8 = scales is not None
+    f = _blocks_fn(name, [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32]
+                   + ([f32, f32] if fp8 else []) + [i32, i32, P, ctypes.c_size_t, i32, P])
+    for n, t in (("out", out), ("query", query)):
+        _cuda(n, t, query.dtype)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, torch.uint8 if fp8 else query.dtype)
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
     for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
@@ -248,13 +239,47 @@ def pa_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, k_cache: tor
             workspace = torch.zeros(need, dtype=torch.uint8, device=query.device)
         _cuda("workspace", workspace)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check("pa_decode_shared_prefix", L.pa_decode_shared_prefix(
+    _check(name, f(
         out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
         block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
         group_start.data_ptr(), prefix_lens.data_ptr(), group_start.numel() - 1,
-        int(max_group_size), B, Hq, Hkv, d, bs, NB, float(scale), int(max_context_len),
-        int(partition_size), ws_ptr or None, ws_bytes, _dtype_code(k_cache), _stream(stream)))
+        int(max_group_size), B, Hq, Hkv, d, bs, NB, float(scale),
+        *([float(scales[0]), float(scales[1])] if fp8 else []), int(max_context_len),
+        int(partition_size), ws_ptr or None, ws_bytes, _dtype_code(query), _stream(stream)))
     return out
+
+
+def pa_decode_shared_prefix(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, group_start: torch.Tensor,
+                            prefix_lens: torch.Tensor, max_group_size: int, scale: float,
+                            max_context_len: int, partition_size: int,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """pa_decode over groups of sequences sharing a prefix in the same
+    physical blocks: ``group_start`` (int32 [num_groups + 1], runs of
+    consecutive sequences covering the batch) and ``prefix_lens`` (int32 [B],
+    shared leading tokens of each sequence, equal within a group) on the
+    device; ``max_group_size`` bounds the groups' sizes.  The shared prefix's
+    K/V is read once per group.  ``workspace`` as for pa_decode."""
+    return _shared_prefix("pa_decode_shared_prefix", out, query, k_cache, v_cache, block_tables,
+                          context_lens, group_start, prefix_lens, max_group_size, scale, None,
+                          max_context_len, partition_size, workspace, stream)
+
+
+def pa_decode_shared_prefix_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                context_lens: torch.Tensor, group_start: torch.Tensor,
+                                prefix_lens: torch.Tensor, max_group_size: int, scale: float,
+                                k_scale: float, v_scale: float, max_context_len: int,
+                                partition_size: int, workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """pa_decode_shared_prefix over uint8 FP8 E4M3 caches (codes times
+    k_scale / v_scale), fp16 or bf16 queries and output."""
+    return _shared_prefix("pa_decode_shared_prefix_fp8", out, query, k_cache, v_cache,
+                          block_tables, context_lens, group_start, prefix_lens, max_group_size,
+                          scale, (k_scale, v_scale), max_context_len, partition_size, workspace,
+                          stream)
 
 
 def pa_decode_reduce(out: torch.Tensor, workspace: torch.Tensor, context_lens: torch.Tensor,
@@ -321,13 +346,11 @@ def _blocks_fn(name: str, argtypes):
     return f
 
 
-def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
-                   stream=None) -> None:
-    """Copy-on-write fork: for each row (src, dst) of ``block_mapping`` (CUDA
-    int64 [n, 2]), physical block dst of both caches becomes a copy of block
-    src.  Destinations distinct and not also sources."""
+def _copy_blocks(name, k_cache, v_cache, block_mapping, dtypes, stream):
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    f = _blocks_fn("pa_copy_blocks", [P, P, P, i32, i32, i32, i32, i64, P])
+    f = _blocks_fn(name, [P, P, P, i32, i32, i32, i32, i64, P])
+    if k_cache.dtype not in dtypes:
+        raise ValueError(f"{name}: caches must be {' or '.join(str(d) for d in dtypes)}")
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _cuda(n, t, k_cache.dtype)
         if not t.is_contiguous():
@@ -338,8 +361,23 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: 
     NB, Hkv, bs, d = k_cache.shape
     if v_cache.shape != k_cache.shape:
         raise ValueError("k_cache and v_cache shapes differ")
-    _check("pa_copy_blocks", f(k_cache.data_ptr(), v_cache.data_ptr(), block_mapping.data_ptr(),
-                               block_mapping.shape[0], Hkv, d, bs, NB, _stream(stream)))
+    _check(name, f(k_cache.data_ptr(), v_cache.data_ptr(), block_mapping.data_ptr(),
+                   block_mapping.shape[0], Hkv, d, bs, NB, _stream(stream)))
+
+
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
+                   stream=None) -> None:
+    """Copy-on-write fork: for each row (src, dst) of ``block_mapping`` (CUDA
+    int64 [n, 2]), physical block dst of both caches (fp16 or bf16) becomes a
+    copy of block src.  Destinations distinct and not also sources."""
+    _copy_blocks("pa_copy_blocks", k_cache, v_cache, block_mapping,
+                 (torch.float16, torch.bfloat16), stream)
+
+
+def pa_copy_blocks_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
+                       stream=None) -> None:
+    """pa_copy_blocks over uint8 FP8 E4M3 caches."""
+    _copy_blocks("pa_copy_blocks_fp8", k_cache, v_cache, block_mapping, (torch.uint8,), stream)
 
 
 def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Tensor,
@@ -428,19 +466,18 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, k_cache: torch.Tensor,
     return out
 
 
-def pa_prefill(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor,
-               k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
-               context_lens: torch.Tensor, scale: float, max_q_len: int,
-               stream=None) -> torch.Tensor:
-    """Causal chunked-prefill attention into ``out`` [total_q, Hq, d]: row t of
-    sequence i's chunk (rows query_start[i]..query_start[i+1]-1) sits at
-    position context_lens[i] - q_len_i + t and attends to tokens 0..that."""
+def _prefill(name, out, query, query_start, k_cache, v_cache, block_tables, context_lens, scale,
+             scales, max_q_len, stream):
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
-    f = _blocks_fn("pa_prefill", [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
-                                  f32, i32, P])
-    dt = k_cache.dtype
-    for n, t in (("out", out), ("query", query), ("k_cache", k_cache), ("v_cache", v_cache)):
-        _cuda(n, t, dt)
+    fp8 = scales is not None
+    f = _blocks_fn(name, [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32]
+                   + ([f32, f32] if fp8 else []) + [i32, P])
+    for n, t in (("out", out), ("query", query)):
+        _cuda(n, t, query.dtype)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda(n, t, torch.uint8 if fp8 else query.dtype)
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
     for n, t in (("query_start", query_start), ("block_tables", block_tables),
@@ -453,11 +490,33 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor
     B = context_lens.numel()
     if query_start.numel() != B + 1 or out.shape != query.shape:
         raise ValueError("query_start must have num_seqs + 1 entries; out must match query")
-    _check("pa_prefill", f(out.data_ptr(), query.data_ptr(), query_start.data_ptr(),
-                           k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-                           block_tables.shape[1], context_lens.data_ptr(), B, int(max_q_len), Hq,
-                           Hkv, d, bs, NB, float(scale), _dtype_code(k_cache), _stream(stream)))
+    _check(name, f(out.data_ptr(), query.data_ptr(), query_start.data_ptr(), k_cache.data_ptr(),
+                   v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                   context_lens.data_ptr(), B, int(max_q_len), Hq, Hkv, d, bs, NB, float(scale),
+                   *([float(scales[0]), float(scales[1])] if fp8 else []), _dtype_code(query),
+                   _stream(stream)))
     return out
+
+
+def pa_prefill(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor,
+               k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, scale: float, max_q_len: int,
+               stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention into ``out`` [total_q, Hq, d]: row t of
+    sequence i's chunk (rows query_start[i]..query_start[i+1]-1) sits at
+    position context_lens[i] - q_len_i + t and attends to tokens 0..that."""
+    return _prefill("pa_prefill", out, query, query_start, k_cache, v_cache, block_tables,
+                    context_lens, scale, None, max_q_len, stream)
+
+
+def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, query_start: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                   max_q_len: int, stream=None) -> torch.Tensor:
+    """pa_prefill over uint8 FP8 E4M3 caches (codes times k_scale / v_scale),
+    fp16 or bf16 queries and output."""
+    return _prefill("pa_prefill_fp8", out, query, query_start, k_cache, v_cache, block_tables,
+                    context_lens, scale, (k_scale, v_scale), max_q_len, stream)
 
 
 def pa_selftest_bounded_wait(stream=None) -> None:

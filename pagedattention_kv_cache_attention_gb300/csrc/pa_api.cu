@@ -40,6 +40,9 @@ cudaError_t error_word(unsigned int **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(int32_t d) { return d == PA_FP16 || d == PA_BF16; }
+bool fp8_scales_ok(float k_scale, float v_scale) {
+  return std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f;
+}
 bool head_dim_ok(int32_t d) { return d == 64 || d == 128; }
 bool block_size_ok(int32_t b) { return b == 16 || b == 32; }
 
@@ -76,7 +79,7 @@ constexpr int32_t kMaxFusedParts = 32;
 
 extern "C" {
 
-int32_t pa_version(void) { return 3; }
+int32_t pa_version(void) { return 4; }
 
 const char *pa_status_string(int32_t status) {
   switch (status) {
@@ -259,7 +262,7 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
         partition_size <= 0 || (num_seqs > 0 && (sp->num_groups > num_seqs ||
                                                  sp->max_group_size > num_seqs)))
       return PA_ERR_INVALID_ARG;
-    if (kv_fp8 || partition_size > pa::kMaxSharedPrefixPartition) return PA_ERR_UNSUPPORTED;
+    if (partition_size > pa::kMaxSharedPrefixPartition) return PA_ERR_UNSUPPORTED;
     const int32_t mpc = pa::shared_prefix_members_per_cta(group);
     chunks = (sp->max_group_size + mpc - 1) / mpc;
     if (static_cast<int64_t>(P) * chunks > 0x7fffffff) return PA_ERR_UNSUPPORTED;
@@ -312,7 +315,7 @@ pa_status decode_impl(void *out, const void *query, const void *k_cache, const v
     a.max_group_size = sp->max_group_size;
     a.members_per_cta = pa::shared_prefix_members_per_cta(group);
     a.chunks = chunks;
-    if (pa::launch_shared_prefix(a, k_cache, v_cache, pool_rows, head_dim, dtype, cs,
+    if (pa::launch_shared_prefix(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8, cs,
                                  &map_failed) != cudaSuccess)
       return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
   }
@@ -358,6 +361,25 @@ pa_status pa_decode_shared_prefix(void *out, const void *query, const void *k_ca
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, max_context_len, partition_size, workspace,
                      workspace_bytes, dtype, false, 1.f, 1.f, stream, &sp);
+}
+
+pa_status pa_decode_shared_prefix_fp8(void *out, const void *query, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      const int32_t *group_start, const int32_t *prefix_lens,
+                                      int32_t num_groups, int32_t max_group_size,
+                                      int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int64_t num_blocks, float scale, float k_scale,
+                                      float v_scale, int32_t max_context_len,
+                                      int32_t partition_size, void *workspace,
+                                      size_t workspace_bytes, int32_t dtype, void *stream) {
+  if (!fp8_scales_ok(k_scale, v_scale) || !dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
+  const SharedPrefix sp{group_start, prefix_lens, num_groups, max_group_size};
+  return decode_impl(out, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, max_context_len, partition_size, workspace,
+                     workspace_bytes, dtype, true, k_scale, v_scale, stream, &sp);
 }
 
 pa_status pa_decode_fp8(void *out, const void *query, const void *k_cache, const void *v_cache,
@@ -417,12 +439,16 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t k
                                                                                   : PA_ERR_CUDA;
 }
 
-pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
-                     const void *k_cache, const void *v_cache, const int32_t *block_tables,
-                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
-                     int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
-                     int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
-                     int32_t dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status prefill_impl(void *out, const void *query, const int32_t *query_start,
+                       const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
+                       int32_t dtype, bool kv_fp8, float k_scale, float v_scale, void *stream) {
   if (num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq <= 0 || !dtype_ok(dtype) || !std::isfinite(scale) ||
       !(scale > 0.f))
@@ -455,18 +481,51 @@ pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
   a.bs_log2 = block_size == 16 ? 4 : 5;
   a.max_q_len = max_q_len;
   a.num_blocks = num_blocks;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale_log2 = scale * 1.4426950408889634f * k_scale;
+  a.out_scale = v_scale;
   a.err = err;
   bool map_failed = false;
-  if (pa::launch_prefill(a, k_cache, v_cache, pool_rows, head_dim, dtype,
+  if (pa::launch_prefill(a, k_cache, v_cache, pool_rows, head_dim, dtype, kv_fp8,
                          static_cast<cudaStream_t>(stream), &map_failed) != cudaSuccess)
     return map_failed ? PA_ERR_INVALID_ARG : PA_ERR_CUDA;
   return PA_OK;
 }
 
-pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
-                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
-                         int32_t block_size, int64_t num_blocks, void *stream) {
+}  // namespace
+
+extern "C" {
+
+pa_status pa_prefill(void *out, const void *query, const int32_t *query_start,
+                     const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                     int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
+                     int32_t dtype, void *stream) {
+  return prefill_impl(out, query, query_start, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                      context_lens, num_seqs, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, dtype, false, 1.f, 1.f, stream);
+}
+
+pa_status pa_prefill_fp8(void *out, const void *query, const int32_t *query_start,
+                         const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                         int32_t max_blocks_per_seq, const int32_t *context_lens,
+                         int32_t num_seqs, int32_t max_q_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int64_t num_blocks, float scale, float k_scale, float v_scale,
+                         int32_t dtype, void *stream) {
+  if (!fp8_scales_ok(k_scale, v_scale)) return PA_ERR_INVALID_ARG;
+  return prefill_impl(out, query, query_start, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                      context_lens, num_seqs, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                      block_size, num_blocks, scale, dtype, true, k_scale, v_scale, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+pa_status copy_blocks_impl(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                           int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int64_t num_blocks, int elem_bytes, void *stream) {
   if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PA_OK;
@@ -481,13 +540,31 @@ pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapp
   a.dst[1] = v_cache;
   a.mapping = block_mapping;
   a.num_pairs = num_pairs;
-  a.block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * 2;
+  a.block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * elem_bytes;
   a.src_blocks = num_blocks;
   a.dst_blocks = num_blocks;
   a.err = err;
   return pa::launch_block_copy(a, 2, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, void *stream) {
+  return copy_blocks_impl(k_cache, v_cache, block_mapping, num_pairs, num_kv_heads, head_dim,
+                          block_size, num_blocks, 2, stream);
+}
+
+pa_status pa_copy_blocks_fp8(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                             int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int64_t num_blocks, void *stream) {
+  return copy_blocks_impl(k_cache, v_cache, block_mapping, num_pairs, num_kv_heads, head_dim,
+                          block_size, num_blocks, 1, stream);
 }
 
 namespace {

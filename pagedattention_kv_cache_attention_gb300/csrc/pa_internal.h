@@ -104,7 +104,8 @@ struct PrefillArgs {
   int max_blocks_per_seq;
   int num_seqs, num_q_heads, num_kv_heads, group, bs_log2, max_q_len;
   int64_t num_blocks;
-  float scale_log2;
+  float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
+  float out_scale;              // V dequantisation scale for FP8 caches, 1 otherwise
   unsigned *err;
   // The shared-prefix pass (the same kernel over a group's shared prefix):
   // rows are (member, query head) pairs of a group's sequences, keys the
@@ -160,18 +161,18 @@ cudaError_t launch_decode(const DecodeArgs &a, const void *k_cache, const void *
                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
                           cudaStream_t stream, bool *map_failed);
 cudaError_t launch_reduce(const ReduceArgs &a, int head_dim, int dtype, cudaStream_t stream);
-// The shared-prefix pass of pa_decode_shared_prefix (16-bit caches); the
-// decode launch with a.prefix_lens set follows it on the same stream.
+// The shared-prefix pass of pa_decode_shared_prefix (16-bit or FP8 caches);
+// the decode launch with a.prefix_lens set follows it on the same stream.
 cudaError_t launch_shared_prefix(const DecodeArgs &a, const void *k_cache, const void *v_cache,
-                                 int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                                 bool *map_failed);
+                                 int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                                 cudaStream_t stream, bool *map_failed);
 // Sequences of one group that a shared-prefix CTA serves at query group size G.
 int shared_prefix_members_per_cta(int group);
 cudaError_t launch_reshape(const ReshapeArgs &a, cudaStream_t stream);
 cudaError_t launch_block_copy(const BlockCopyArgs &a, int num_tensors, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,
-                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                           bool *map_failed);
+                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                           cudaStream_t stream, bool *map_failed);
 
 // The host-side checks of pa_decode that come before the workspace check;
 // returns a pa_status value (PA_OK when pa_decode would go on to the workspace).

@@ -127,17 +127,63 @@ struct PairLayout {
   static constexpr int kKOff = TILES * kAtoms * kPairQAtom;         // K ring: [SK][atoms]
   static constexpr int kVOff = kKOff + SK * kAtoms * kPairKvAtom;   // V ring: [SV][atoms]
   static constexpr int kBarOff = kVOff + SV * kAtoms * kPairKvAtom;
-  static constexpr int kBars = 2 * SK + 2 * SV + 1 + 2 + 2 + 4 + 4 + 1;
-  static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + 16;
+  // + the FP8 landing barriers (SK + SV) and the V sub-tile masks (SV words)
+  static constexpr int kBars = 2 * SK + 2 * SV + 1 + 2 + 2 + 4 + 4 + 1 + SK + SV;
+  static constexpr size_t kSmem = 1024 + kBarOff + kBars * 8 + SV * 4 + 16;
 };
 
-template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX>
+// FP8 E4M3 caches: a step's codes (64 rows of D bytes, in the pool map's
+// swizzle: 16-byte unit c of row r at unit c ^ (r & 7) for 128-byte rows,
+// c ^ ((r >> 1) & 3) for 64-byte rows) are copied into the upper half of the
+// fp16 stage, and one warp widens them there to the fp16 tile the MMA reads
+// (128-byte rows of 64 dims per atom, unit k of row r at k ^ (r & 7)); every
+// code is exact in fp16.  Each pass reads 1 KB of codes into registers
+// before it writes: at head_dim 128 the codes of row r share their 128 bytes
+// with row r of the second atom only, and at head_dim 64 a pass writes over
+// codes of that pass or of earlier ones only, so nothing is overwritten
+// before it is read.
+template <int D>
+__device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
+  constexpr int kRows = 1024 / D;      // rows per pass: 8 (d 128) or 16 (d 64)
+  constexpr int kPerRow = 32 / kRows;  // lanes per row: 4 or 2
+  const uint8_t *codes = st + (D / 64) * kPairKvAtom / 2;
+#pragma unroll 1
+  for (int j = 0; j < kPairKeys / kRows; ++j) {
+    const int r = j * kRows + lane / kPerRow;
+    const int c0 = 2 * (lane % kPerRow);  // this lane's 16-dim units c0 and c0 + 1
+    const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
+    const uint4 x0 = *reinterpret_cast<const uint4 *>(codes + r * D + ((c0 ^ sw) << 4));
+    const uint4 x1 = *reinterpret_cast<const uint4 *>(codes + r * D + (((c0 + 1) ^ sw) << 4));
+    __syncwarp();
+    uint32_t h0[8], h1[8];
+    e4m3x16_to_half(x0, h0);
+    e4m3x16_to_half(x1, h1);
+    // unit c (dims 16 c .. 16 c + 15) becomes fp16 units 2 (c & 3) and
+    // 2 (c & 3) + 1 of atom c / 4
+    uint8_t *row = st + (c0 >> 2) * kPairKvAtom + r * 128;
+    const int k0 = 2 * (c0 & 3);
+    *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+    *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ (r & 7)) << 4)) =
+        make_uint4(h0[4], h0[5], h0[6], h0[7]);
+    *reinterpret_cast<uint4 *>(row + (((k0 + 2) ^ (r & 7)) << 4)) =
+        make_uint4(h1[0], h1[1], h1[2], h1[3]);
+    *reinterpret_cast<uint4 *>(row + (((k0 + 3) ^ (r & 7)) << 4)) =
+        make_uint4(h1[4], h1[5], h1[6], h1[7]);
+    __syncwarp();
+  }
+}
+
+// F8: the caches hold FP8 E4M3 codes, widened to fp16 in shared memory; the
+// products then run in fp16 whatever T is (bf16 queries are carried in fp16,
+// see the Q load).
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX, bool F8>
 __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
   static_assert(!PX || TILES == 1, "the shared-prefix pass runs one tile per CTA");
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(!F8 || !SPLIT, "FP8 caches: the products run in fp16 (no split P)");
   using L = PairLayout<SK, SV, TILES, D>;
   constexpr int kAtoms = L::kAtoms;
   constexpr int kIssue0 = 4 * TILES;      // first MMA-issuing warp
@@ -145,6 +191,9 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+  // MMA operand type (P included): T, or fp16 over FP8 caches
+  using MT = typename std::conditional<F8, __half, T>::type;
+  constexpr bool kMmaBf16 = kBf16 && !F8;
   // TMEM columns of a tile: scores 0..63, P 64..127, O from 128.  fp16 P: two
   // buffers of 32 columns (step n in buffer n % 2); bf16 P: one buffer, hi
   // parts in 64..95 and lo parts in 96..127.
@@ -164,7 +213,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   uint64_t *p_full = s_free + 2;       // [2 tiles][2 P buffers]
   uint64_t *pv_done = p_full + 4;      // [2 tiles][2 P buffers]
   uint64_t *q_ready = pv_done + 4;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_ready + 1);
+  uint64_t *k_land = q_ready + 1;      // [SK] FP8: a K step's codes are in
+  uint64_t *v_land = k_land + SK;      // [SV] FP8: a V step's codes are in
+  uint32_t *v_masks = reinterpret_cast<uint32_t *>(v_land + SV);  // [SV] FP8: loaded sub-tiles
+  uint32_t *tmem_slot = v_masks + SV;
 
   const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -194,6 +246,8 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_ready, TILES * kTcRows);
+    for (int s = 0; s < SK; ++s) mbar_init(&k_land[s], 1);
+    for (int s = 0; s < SV; ++s) mbar_init(&v_land[s], 1);
     fence_barrier_init();
   }
   if (warp == kIssue0) tmem_alloc(tmem_slot, 256 * TILES);
@@ -316,15 +370,49 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     const bool row_ok = tok <= t_last;
     const int pos = PX ? n_keys - 1 : base_pos + tok;  // keys up to pos are attended to
     const int my_steps = t == 0 ? n_steps0 : n_steps1;
+    float sl2 = a.scale_log2;  // this row's softmax scale (base 2)
     {
       const T *qrow = static_cast<const T *>(a.query) +
                       (static_cast<int64_t>(q0 + (row_ok ? tok : 0)) * a.num_q_heads + kvh * G +
                        rc % G) * D;
       uint8_t *qt = smem + L::kQOff + t * kAtoms * kPairQAtom;
+      // bf16 queries over FP8 caches: the row is scaled by 2^e so that its
+      // largest magnitude lands in [2^14, 2^15), then rounded to fp16 (exact
+      // for every value down to 2^-31 of the largest: bf16 carries 8
+      // significant bits, and fp16 holds 8 bits at every magnitude from 2^-17
+      // up), and 2^-e joins the row's softmax scale
+      float qf = 1.f;
+      if constexpr (F8 && kBf16) {
+        float mx = 0.f;
+        if (row_ok) {
+#pragma unroll 4
+          for (int ch = 0; ch < D / 8; ++ch) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(qrow + ch * 8);
+#pragma unroll
+            for (int w2 = 0; w2 < 4; ++w2) {
+              const float2 f = Elem<T>::unpack(word_of(v, w2));
+              mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+        }
+        const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+        const int e = min(120, 14 - ex);
+        qf = ldexpf(1.f, e);
+        sl2 = ldexpf(sl2, -e);
+      }
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {
-        const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
-                               : make_uint4(0, 0, 0, 0);
+        uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qrow + ch * 8)
+                         : make_uint4(0, 0, 0, 0);
+        if constexpr (F8 && kBf16) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int w2 = 0; w2 < 4; ++w2) {
+            const float2 f = Elem<T>::unpack(word_of(v, w2));
+            w4[w2] = Elem<__half>::pack(f.x * qf, f.y * qf);
+          }
+          v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
         *reinterpret_cast<uint4 *>(qt + (ch >> 3) * kPairQAtom + r * 128 +
                                    (((ch & 7) ^ (r & 7)) << 4)) = v;
       }
@@ -398,7 +486,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       t8[7] = t22[21];
       const float tmax_raw = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
                                    fmaxf(t8[6], t8[7]));
-      const float tmax = tmax_raw * a.scale_log2;  // the scale is positive: same order
+      const float tmax = tmax_raw * sl2;  // the scale is positive: same order
       const float m_new = fmaxf(m_ref, tmax);
       const bool move = m_new > m_ref + kRescaleLog2;  // includes the first finite max
       const float alpha = !move ? 1.f : (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - m_new));
@@ -409,7 +497,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
       // P for the whole step in registers first (s scale - m and the row sum on
       // packed fp32 pairs), so the wait for its buffer below overlaps the math
-      const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t scale2 = f2_pack(sl2, sl2);
       const uint64_t negm2 = f2_pack(neg_m, neg_m);
       uint64_t ls2[4] = {0, 0, 0, 0};  // +0.0f pairs
       uint32_t ph[kPairKeys / 2], pl[SPLIT ? kPairKeys / 2 : 1];
@@ -418,10 +506,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         const float2 x = f2_unpack(f2_fma(f2_pack(sv[2 * e], sv[2 * e + 1]), scale2, negm2));
         const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
         ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
-        ph[e] = Elem<T>::pack(p0, p1);
+        ph[e] = Elem<MT>::pack(p0, p1);
         if constexpr (SPLIT) {
-          const float2 h = Elem<T>::unpack(ph[e]);
-          pl[e] = Elem<T>::pack(p0 - h.x, p1 - h.y);
+          const float2 h = Elem<MT>::unpack(ph[e]);
+          pl[e] = Elem<MT>::pack(p0 - h.x, p1 - h.y);
         }
       }
       {
@@ -479,7 +567,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       const int last = my_steps - 1;
       if (__all_sync(kFullMask, mbar_wait_bounded(&pv_done[2 * t + last % kPBufs], (last / kPBufs) & 1))) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? a.out_scale / l : 0.f;  // times the V scale (FP8)
         const int64_t orow_idx = static_cast<int64_t>(q0 + tok) * a.num_q_heads + kvh * G + rc % G;
         if constexpr (PX) {
           // the partition's partial of this row, for a member that takes the
@@ -544,7 +632,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       const uint32_t tt = tmem + t * 256;
       bool ok_run = true;
       if (qk_role) {
-        const uint32_t id_qk = umma_idesc_f16(kBf16 ? 1 : 0, false, kTcRows, kPairKeys);
+        const uint32_t id_qk = umma_idesc_f16(kMmaBf16 ? 1 : 0, false, kTcRows, kPairKeys);
         const uint32_t qb = smem_addr(smem + L::kQOff) + t * kAtoms * kPairQAtom;
         const uint32_t sk0 = smem_addr(smem + L::kKOff);
         // descriptors of the tile's Q and of K stage 0; every other operand
@@ -581,7 +669,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
           mbar_arrive(&k_empty[m % SK]);
         }
       } else {
-        const uint32_t id_pv = umma_idesc_f16(kBf16 ? 1 : 0, true, kTcRows, D);
+        const uint32_t id_pv = umma_idesc_f16(kMmaBf16 ? 1 : 0, true, kTcRows, D);
         const uint32_t sv0 = smem_addr(smem + L::kVOff);
         const uint64_t dv0 = umma_desc_sw128(sv0, kPairKvAtom, 1024);  // V stage 0, as for K
         for (int n = 0; n < nt && ok_run; ++n) {
@@ -633,6 +721,80 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     int win_base = 0;
     int win = block_of(lane);
     bool ok_run = true;
+    if constexpr (F8) {
+      // A step's copies (16 rows of head_dim codes per sub-tile) land in the
+      // upper half of its stage; the warp widens a step to fp16 S - 1 steps
+      // after issuing its copies (so S - 1 steps of copies stay in flight),
+      // clears what V must not contribute, and hands the stage over.
+      constexpr int kF8Sub = 16 * D;                // bytes of one sub-tile's codes
+      constexpr int kStage = kAtoms * kPairKvAtom;  // bytes of one fp16 stage
+      const int S = k_role ? SK : SV;
+      uint64_t *land = k_role ? k_land : v_land;
+      uint64_t *full = k_role ? k_full : v_full;
+      uint64_t *empty = k_role ? k_empty : v_empty;
+      uint8_t *ring = smem + (k_role ? L::kKOff : L::kVOff);
+      const CUtensorMap *map = k_role ? &kmap : &vmap;
+      for (int n = 0; n < n_steps + S - 1 && ok_run; ++n) {
+        if (n < n_steps) {
+          if (n * kSub >= win_base + 32) {
+            win_base += 32;
+            win = block_of(win_base + lane);
+          }
+          const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
+          const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
+          const int s = n % S;
+          if (lane == 0) {
+            if (n >= S && !mbar_wait_bounded(&empty[s], ((n / S) - 1) & 1)) {
+              ok_run = false;
+            } else {
+              if (!k_role) v_masks[s] = mask;
+              if (mask == 0)
+                mbar_arrive(&land[s]);
+              else
+                mbar_arrive_expect_tx(&land[s], __popc(mask) * kF8Sub);
+            }
+          }
+          ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+          if (!ok_run) break;
+          __syncwarp();
+          if (lane < kSub && my_phys >= 0) {
+            const int u = n * kSub + lane;
+            const int y =
+                ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((key_base + u * 16) & bs_mask);
+            tma_load_2d(ring + s * kStage + kStage / 2 + lane * kF8Sub, map, 0, y, &land[s],
+                        policy);
+          }
+        }
+        const int m = n - (S - 1);
+        if (m < 0) continue;
+        const int s = m % S;
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(&land[s], (m / S) & 1);
+        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          ok_run = false;
+          break;
+        }
+        uint8_t *st = ring + s * kStage;
+        f8_stage_to_f16<D>(st, lane);
+        if (!k_role) {
+          // V rows past n_keys and of sub-tiles not loaded become zeros
+          const uint32_t vm = v_masks[s];
+          const int first = n_keys - m * kPairKeys;  // first row to clear
+          if (vm != kAllSub || first < kPairKeys) {
+            for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {  // 16-byte units
+              const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
+              if (row >= first || !((vm >> (row >> 4)) & 1u))
+                *reinterpret_cast<uint4 *>(st + b * kPairKvAtom + row * 128 + u16 * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+    } else {
     for (int n = 0; n < n_steps && ok_run; ++n) {
       if (n * kSub >= win_base + 32) {
         win_base += 32;
@@ -726,6 +888,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
         if (lane == 0) mbar_arrive(&v_full[sv]);
       }
     }
+    }
     if (!ok_run && lane == 0) atomicOr(a.err, kErrTimeout);
   }
 
@@ -741,14 +904,15 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   grid_launch_dependents();
 }
 
-template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX = false>
+template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX = false,
+          bool F8 = false>
 cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km,
                                      const CUtensorMap &vm, cudaStream_t stream) {
   // the shared-prefix pass keeps each member's first partition and the pass's
   // control words after the barriers
   constexpr size_t smem = PairLayout<SK, SV, TILES, D>::kSmem + (PX ? (kTcRows + 8) * 4 : 0);
   static_assert(smem <= (TILES == 1 ? 113 : 227) * 1024, "shared memory");
-  auto kern = pa_prefill_tc_pair_kernel<T, D, SK, SV, SPLIT, TILES, PX>;
+  auto kern = pa_prefill_tc_pair_kernel<T, D, SK, SV, SPLIT, TILES, PX, F8>;
   static SmemLimitOnce smem_limit;
   const cudaError_t e = smem_limit.ensure(kern, smem);
   if (e != cudaSuccess) return e;
@@ -788,8 +952,22 @@ namespace {
 
 template <int D>
 cudaError_t launch_prefill_tc_d(const PrefillArgs &a, const CUtensorMap &km,
-                                const CUtensorMap &vm, int dtype, cudaStream_t stream) {
+                                const CUtensorMap &vm, int dtype, bool kv_fp8,
+                                cudaStream_t stream) {
   const bool pair = static_cast<int64_t>(a.max_q_len) * a.group > kTcRows;
+  constexpr int PK = PA_PREFILL_PAIR_KSTAGES, PV = PA_PREFILL_PAIR_VSTAGES;
+  constexpr int SK = PA_PREFILL_SOLO_KSTAGES, SV = PA_PREFILL_SOLO_VSTAGES;
+  if (kv_fp8) {
+    if (dtype == 0)
+      return pair ? launch_prefill_tc_pair_t<__half, D, PK, PV, false, 2, false, true>(a, km, vm,
+                                                                                       stream)
+                  : launch_prefill_tc_pair_t<__half, D, SK, SV, false, 1, false, true>(a, km, vm,
+                                                                                       stream);
+    return pair ? launch_prefill_tc_pair_t<__nv_bfloat16, D, PK, PV, false, 2, false, true>(
+                      a, km, vm, stream)
+                : launch_prefill_tc_pair_t<__nv_bfloat16, D, SK, SV, false, 1, false, true>(
+                      a, km, vm, stream);
+  }
   if (dtype == 0) {
     if (pair)
       return launch_prefill_tc_pair_t<__half, D, PA_PREFILL_PAIR_KSTAGES, PA_PREFILL_PAIR_VSTAGES,
@@ -810,19 +988,19 @@ cudaError_t launch_prefill_tc_d(const PrefillArgs &a, const CUtensorMap &km,
 // 128-row tile run with two tiles per CTA (one CTA per SM); shorter ones
 // (short chunks, decode-like rows) with one tile per CTA, two CTAs per SM.
 cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void *v_cache,
-                           int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                           bool *map_failed) {
+                           int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                           cudaStream_t stream, bool *map_failed) {
   CUtensorMap km, vm;
   *map_failed = false;
-  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, false) ||
-      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, false)) {
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, kv_fp8) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, kv_fp8)) {
     *map_failed = true;
     return cudaErrorInvalidValue;
   }
   if (a.max_q_len == 0) return cudaSuccess;
   if (!prefill_tc_supported(head_dim, a.group)) return cudaErrorInvalidValue;
-  return head_dim == 128 ? launch_prefill_tc_d<128>(a, km, vm, dtype, stream)
-                         : launch_prefill_tc_d<64>(a, km, vm, dtype, stream);
+  return head_dim == 128 ? launch_prefill_tc_d<128>(a, km, vm, dtype, kv_fp8, stream)
+                         : launch_prefill_tc_d<64>(a, km, vm, dtype, kv_fp8, stream);
 }
 
 // The shared-prefix pass of pa_decode_shared_prefix on the same kernel: one
@@ -832,12 +1010,12 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *k_cache, const void
 int shared_prefix_members_per_cta(int group) { return kTcRows / group; }
 
 cudaError_t launch_shared_prefix(const DecodeArgs &d, const void *k_cache, const void *v_cache,
-                                 int64_t pool_rows, int head_dim, int dtype, cudaStream_t stream,
-                                 bool *map_failed) {
+                                 int64_t pool_rows, int head_dim, int dtype, bool kv_fp8,
+                                 cudaStream_t stream, bool *map_failed) {
   CUtensorMap km, vm;
   *map_failed = false;
-  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, false) ||
-      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, false)) {
+  if (!encode_pool_map(&km, k_cache, pool_rows, head_dim, dtype, kv_fp8) ||
+      !encode_pool_map(&vm, v_cache, pool_rows, head_dim, dtype, kv_fp8)) {
     *map_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -853,6 +1031,7 @@ cudaError_t launch_shared_prefix(const DecodeArgs &d, const void *k_cache, const
   a.bs_log2 = d.bs_log2;
   a.num_blocks = d.num_blocks;
   a.scale_log2 = d.scale_log2;
+  a.out_scale = d.out_scale;
   a.err = d.err;
   a.ws_m = d.ws_m;
   a.ws_l = d.ws_l;
@@ -867,6 +1046,19 @@ cudaError_t launch_shared_prefix(const DecodeArgs &d, const void *k_cache, const
   a.num_parts = d.num_parts;
   a.max_context_len = d.max_context_len;
   constexpr int KS = PA_PREFILL_SOLO_KSTAGES, VS = PA_PREFILL_SOLO_VSTAGES;
+  if (kv_fp8) {
+    if (dtype == 0)
+      return head_dim == 128
+                 ? launch_prefill_tc_pair_t<__half, 128, KS, VS, false, 1, true, true>(a, km, vm,
+                                                                                       stream)
+                 : launch_prefill_tc_pair_t<__half, 64, KS, VS, false, 1, true, true>(a, km, vm,
+                                                                                      stream);
+    return head_dim == 128
+               ? launch_prefill_tc_pair_t<__nv_bfloat16, 128, KS, VS, false, 1, true, true>(
+                     a, km, vm, stream)
+               : launch_prefill_tc_pair_t<__nv_bfloat16, 64, KS, VS, false, 1, true, true>(
+                     a, km, vm, stream);
+  }
   if (dtype == 0)
     return head_dim == 128
                ? launch_prefill_tc_pair_t<__half, 128, KS, VS, false, 1, true>(a, km, vm, stream)

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
-    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 3 ? 0 : 1;}\n')
+    src.write_text('#include "pa.h"\nint main(void){return pa_version() == 4 ? 0 : 1;}\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
                     "-I", os.path.join(ROOT, "include"), str(src)], check=True)
 
@@ -121,7 +121,7 @@ def test_reshape_host_validation(lib):
 
 
 def test_version(lib):
-    assert lib.pa_version() == 3
+    assert lib.pa_version() == 4
 
 
 def _shared_prefix_status(lib, **over):
@@ -152,3 +152,47 @@ def _shared_prefix_status(lib, **over):
 ])
 def test_shared_prefix_host_validation(lib, over, status):
     assert _shared_prefix_status(lib, **over) == status
+
+
+def _fp8_status(lib, name, **over):
+    """Host checks of the FP8 entry points (bad scales, then the checks of
+    their 16-bit forms); nothing is dereferenced."""
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    fake = P(0x10000)
+    if name == "pa_prefill_fp8":
+        args = dict(out=fake, q=fake, qs=fake, k=fake, v=fake, bt=fake, mb=64, cl=fake, B=4,
+                    mq=64, Hq=32, Hkv=8, d=128, bs=16, NB=1024, scale=0.088, ks=0.5, vs=0.5, dt=0,
+                    st=None)
+        types = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64, f32, f32, f32, i32, P]
+    elif name == "pa_decode_shared_prefix_fp8":
+        args = dict(out=fake, q=fake, k=fake, v=fake, bt=fake, mb=160, cl=fake, gs=fake, pl=fake,
+                    ng=4, mgs=8, B=32, Hq=32, Hkv=8, d=128, bs=16, NB=4096, scale=0.088, ks=0.5,
+                    vs=0.5, maxctx=2560, ps=512, ws=fake, wsb=1 << 30, dt=0, st=None)
+        types = [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32, f32, f32,
+                 i32, i32, P, ctypes.c_size_t, i32, P]
+    else:  # pa_copy_blocks_fp8
+        args = dict(k=fake, v=fake, m=fake, n=2, Hkv=8, d=128, bs=16, NB=1024, st=None)
+        types = [P, P, P, i32, i32, i32, i32, i64, P]
+    args.update(over)
+    f = getattr(lib, name)
+    f.argtypes = types
+    f.restype = i32
+    return f(*args.values())
+
+
+@pytest.mark.parametrize("name,over,status", [
+    ("pa_prefill_fp8", dict(ks=0.0), 1), ("pa_prefill_fp8", dict(vs=float("nan")), 1),
+    ("pa_prefill_fp8", dict(ks=float("inf")), 1), ("pa_prefill_fp8", dict(dt=2), 1),
+    ("pa_prefill_fp8", dict(d=96), 2), ("pa_prefill_fp8", dict(Hq=72, Hkv=8), 2),
+    ("pa_prefill_fp8", dict(B=0), 0),
+    ("pa_decode_shared_prefix_fp8", dict(vs=-1.0), 1),
+    ("pa_decode_shared_prefix_fp8", dict(ks=float("nan")), 1),
+    ("pa_decode_shared_prefix_fp8", dict(dt=5), 1),
+    ("pa_decode_shared_prefix_fp8", dict(gs=None), 1),
+    ("pa_decode_shared_prefix_fp8", dict(ps=16384, maxctx=65536), 2),
+    ("pa_decode_shared_prefix_fp8", dict(B=0, ng=1, mgs=1), 0),
+    ("pa_copy_blocks_fp8", dict(d=96), 2), ("pa_copy_blocks_fp8", dict(m=None), 1),
+    ("pa_copy_blocks_fp8", dict(n=0), 0),
+])
+def test_fp8_entry_points_host_validation(lib, name, over, status):
+    assert _fp8_status(lib, name, **over) == status

@@ -51,6 +51,30 @@ def test_copy_blocks_bitexact(pa, name, kw):
     assert np.array_equal(u16(kc), kh) and np.array_equal(u16(vc), vh)
 
 
+@pytest.mark.parametrize("name,kw", [("llama3_70b_cb", dict(batch=16)),
+                                     ("llama3_8b_gqa", dict(batch=8, head_dim=64))])
+def test_copy_blocks_fp8_bitexact(pa, name, kw):
+    """FP8 caches (one byte per element): every pair is copied whole and no
+    byte outside the destination blocks changes -- in particular the last
+    blocks of the pool, which a copy sized for two-byte elements would run
+    past."""
+    w = W.to_fp8(W.make(name, 33, **kw))
+    rng = np.random.default_rng(1)
+    m = _pairs(rng, w.num_blocks, min(40, w.num_blocks // 2))
+    m[0] = [w.num_blocks - 1, m[0, 1]]          # the pool's last block as a source ...
+    m[1] = [m[1, 0], w.num_blocks - 2]          # ... and a block near the end as a destination
+    assert len(set(m[:, 1])) == len(m) and not set(m[:, 1]) & set(m[:, 0])
+    kc, vc = w.k_cache.cuda(), w.v_cache.cuda()
+    pa.pa_copy_blocks_fp8(kc, vc, torch.from_numpy(m).cuda())
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() == 0
+    kh, vh = w.k_cache.numpy().copy(), w.v_cache.numpy().copy()
+    oracle.copy_blocks(kh, vh, m)
+    assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
+    with pytest.raises(ValueError):
+        pa.pa_copy_blocks(kc, vc, torch.from_numpy(m).cuda())   # the 16-bit form refuses uint8
+
+
 def test_fork_then_write_leaves_sharer_unchanged(pa):
     """Sequences of a group share their prefix blocks.  Sequence 1 forks one
     shared block into a free block: with the same data behind a new id every

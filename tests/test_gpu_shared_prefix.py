@@ -53,33 +53,55 @@ class SharedRun:
                  max_group_size=None, block_tables=None, plain=True):
         dev = torch.device("cuda")
         self.w = w
+        self.fp8 = w.kv_dtype == "e4m3"
         self.cl_host = w.context_lens if context_lens is None else context_lens
         self.bt_host = w.block_tables if block_tables is None else block_tables
         self.kc, self.vc = w.k_cache.to(dev), w.v_cache.to(dev)
-        pa.pa_reshape_and_cache(w.key.to(dev), w.value.to(dev), self.kc, self.vc,
-                                w.slot_mapping.to(dev))
+        if self.fp8:
+            pa.pa_reshape_and_cache_fp8(w.key.to(dev), w.value.to(dev), self.kc, self.vc,
+                                        w.slot_mapping.to(dev), w.k_scale, w.v_scale)
+        else:
+            pa.pa_reshape_and_cache(w.key.to(dev), w.value.to(dev), self.kc, self.vc,
+                                    w.slot_mapping.to(dev))
         q, bt, cl = w.query.to(dev), self.bt_host.to(dev), self.cl_host.to(dev)
         gs = (w.group_start if group_start is None else group_start).to(dev)
         pl = (w.prefix_lens if prefix_lens is None else prefix_lens).to(dev)
         mgs = w.max_group_size if max_group_size is None else max_group_size
         self.maxctx = max(int(self.cl_host.max().item()), 1)
         ws = pa.new_decode_workspace(w.num_seqs, w.num_q_heads, w.head_dim, self.maxctx, ps)
+        def shared(out):
+            if self.fp8:
+                pa.pa_decode_shared_prefix_fp8(out, q, self.kc, self.vc, bt, cl, gs, pl, mgs,
+                                               w.scale, w.k_scale, w.v_scale, self.maxctx, ps,
+                                               workspace=ws)
+            else:
+                pa.pa_decode_shared_prefix(out, q, self.kc, self.vc, bt, cl, gs, pl, mgs,
+                                           w.scale, self.maxctx, ps, workspace=ws)
         self.out = torch.empty_like(q)
-        pa.pa_decode_shared_prefix(self.out, q, self.kc, self.vc, bt, cl, gs, pl, mgs, w.scale,
-                                   self.maxctx, ps, workspace=ws)
+        shared(self.out)
         # a second call on the same workspace (its join counters left at zero)
         self.out2 = torch.empty_like(q)
-        pa.pa_decode_shared_prefix(self.out2, q, self.kc, self.vc, bt, cl, gs, pl, mgs, w.scale,
-                                   self.maxctx, ps, workspace=ws)
+        shared(self.out2)
         self.plain = None
         if plain:
             self.plain = torch.empty_like(q)
-            pa.pa_decode(self.plain, q, self.kc, self.vc, bt, cl, w.scale, self.maxctx, ps)
+            if self.fp8:
+                pa.pa_decode_fp8(self.plain, q, self.kc, self.vc, bt, cl, w.scale, w.k_scale,
+                                 w.v_scale, self.maxctx, ps)
+            else:
+                pa.pa_decode(self.plain, q, self.kc, self.vc, bt, cl, w.scale, self.maxctx, ps)
         torch.cuda.synchronize()
         self.err = pa.pa_device_errors()
 
     def oracle_out(self, pairs=None):
         w = self.w
+        if self.fp8:
+            kh, vh = w.k_cache.numpy().copy(), w.v_cache.numpy().copy()
+            oracle.reshape_and_cache_fp8(w.key, w.value, kh, vh, w.slot_mapping, w.dtype,
+                                         w.k_scale, w.v_scale)
+            return oracle.decode(w.query, kh, vh, self.bt_host, self.cl_host, w.scale, w.dtype,
+                                 pairs=pairs, kv_dtype="e4m3", k_scale=w.k_scale,
+                                 v_scale=w.v_scale)
         kh, vh = u16(w.k_cache).copy(), u16(w.v_cache).copy()
         oracle.reshape_and_cache(w.key, w.value, kh, vh, w.slot_mapping)
         return oracle.decode(w.query, kh, vh, self.bt_host, self.cl_host, w.scale, w.dtype,
@@ -124,6 +146,43 @@ def test_shared_prefix_matches_oracle(pa, case):
     r = SharedRun(pa, w, ps)
     assert r.err == 0
     r.check(f"groups {ng}x{gs} prefix {P} ps {ps} G {hq // hkv} d {d} bs {bs} {dt}")
+
+
+FP8_CASES = [
+    (3, 2, 256, 40, 64, 32, 8, 128, 16, "fp16"),     # G 4
+    (2, 5, 300, 64, 64, 32, 8, 128, 16, "bf16"),     # two own partitions: the counter join
+    (2, 18, 192, 50, 64, 64, 8, 128, 32, "fp16"),    # G 8, bs 32, two chunks
+    (3, 4, 160, 20, 32, 8, 8, 64, 16, "bf16"),       # MHA, head_dim 64
+    (2, 27, 144, 30, 48, 40, 8, 128, 16, "bf16"),    # G 5, 48-token partitions
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[f"fp8-case{i}" for i in range(len(FP8_CASES))])
+def test_shared_prefix_fp8_matches_oracle(pa, case):
+    """FP8 caches: the shared pass widens the prefix codes in shared memory;
+    every output against the oracle reading the same codes, and against
+    pa_decode_fp8."""
+    ng, gs, P, smax, ps, hq, hkv, d, bs, dt = case
+    w = W.to_fp8(W.make("shared_prefix_cow", seed=51 + ng * gs, groups=ng, group_size=gs,
+                        prefix_len=P, max_len=smax, num_q_heads=hq, num_kv_heads=hkv,
+                        head_dim=d, block_size=bs, dtype=dt, partition_size=ps))
+    r = SharedRun(pa, w, ps)
+    assert r.err == 0
+    r.check(f"FP8 groups {ng}x{gs} prefix {P} ps {ps} G {hq // hkv} d {d} bs {bs} {dt}")
+
+
+def test_full_size_shared_prefix_batch_fp8(pa):
+    """The copy-on-write batch at full size over FP8 caches, bf16 queries: a
+    sample of sequences against the oracle, every output against
+    pa_decode_fp8."""
+    w = W.to_fp8(W.make("shared_prefix_cow", dtype="bf16"))
+    r = SharedRun(pa, w, w.partition_size)
+    assert r.err == 0
+    seqs = [0, 9, 64, 127]
+    r.check("full-size FP8 shared-prefix batch",
+            pairs=[(i, h) for i in seqs for h in range(w.num_q_heads)])
+    diff = (r.out.float() - r.plain.float()).abs()
+    assert (diff <= ATOL + RTOL * r.plain.float().abs()).all()
 
 
 def test_members_shorter_than_the_prefix(pa):
