@@ -372,8 +372,8 @@ class Step:
         import torch
         self.pa, self.w, self.dev = pa, w, dev
         self.fp8 = w.kv_dtype == "e4m3"
-        if shared and (w.group_start is None or self.fp8):
-            raise ValueError("the shared-prefix decode needs a 16-bit workload with prefix groups")
+        if shared and w.group_start is None:
+            raise ValueError("the shared-prefix decode needs a workload with prefix groups")
         self.shared = shared
         if shared:
             self.gs, self.pl = w.group_start.to(dev), w.prefix_lens.to(dev)
@@ -403,7 +403,12 @@ class Step:
         shared-prefix call (default: the resident copies)."""
         w, pa = self.w, self.pa
         out = self.out if out is None else out
-        if self.fp8:
+        if self.fp8 and self.shared:
+            gs, pl = groups if groups is not None else (self.gs, self.pl)
+            pa.pa_decode_shared_prefix_fp8(out, qq, self.kc, self.vc, tables, lens, gs, pl,
+                                           w.max_group_size, w.scale, w.k_scale, w.v_scale,
+                                           self.maxctx, self.ps, workspace=self.ws, stream=st)
+        elif self.fp8:
             pa.pa_decode_fp8(out, qq, self.kc, self.vc, tables, lens, w.scale, w.k_scale,
                              w.v_scale, self.maxctx, self.ps, workspace=self.ws, stream=st)
         elif self.shared:
@@ -736,7 +741,8 @@ def run_ours(args):
                 "step_gbs": round(job_throughput(world, ab["step_unique"], ms_per_step), 2),
                 "hbm_fraction": round(job_throughput(world, ab["step_unique"], ms_per_step)
                                       / world / peak, 4),
-                "decode": "pa_decode_shared_prefix" if S.shared else "pa_decode"},
+                "decode": ("pa_decode_shared_prefix" if S.shared else "pa_decode")
+                          + ("_fp8" if fp8 else "")},
             "roofline": {"bound": "hbm",
                          "kernel": ("pa_decode_shared_prefix call (shared-prefix kernel + decode "
                                     "kernel; the LSE join runs in the latter), bytes of distinct "
@@ -864,15 +870,25 @@ def run_prefill(args):
     dev = torch.device("cuda", 0)
     pw = workloads.make_prefill(args.workload, seed=args.seed, chunk=args.chunk,
                                 **shape_overrides(args))
+    fp8 = args.kv_dtype == "e4m3"
+    if fp8:
+        pw = workloads.to_fp8(pw)
     kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
     key, value, sm = pw.key.to(dev), pw.value.to(dev), pw.slot_mapping.to(dev)
     q, qs = pw.query.to(dev), pw.query_start.to(dev)
     bt, cl = pw.block_tables.to(dev), pw.context_lens.to(dev)
     out = torch.empty_like(q)
-    pa.pa_reshape_and_cache(key, value, kc, vc, sm)
+    if fp8:
+        pa.pa_reshape_and_cache_fp8(key, value, kc, vc, sm, pw.k_scale, pw.v_scale)
+    else:
+        pa.pa_reshape_and_cache(key, value, kc, vc, sm)
 
     def call():
-        pa.pa_prefill(out, q, qs, kc, vc, bt, cl, pw.scale, pw.max_q_len)
+        if fp8:
+            pa.pa_prefill_fp8(out, q, qs, kc, vc, bt, cl, pw.scale, pw.k_scale, pw.v_scale,
+                              pw.max_q_len)
+        else:
+            pa.pa_prefill(out, q, qs, kc, vc, bt, cl, pw.scale, pw.max_q_len)
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize(dev)
@@ -888,6 +904,7 @@ def run_prefill(args):
     fl = prefill_flops(pw)
     print(json.dumps({"op": "prefill", "workload": pw.name, "chunk": args.chunk,
                       "seqs": pw.num_seqs, "total_q": pw.total_q, "dtype": pw.dtype,
+                      "kv_dtype": pw.kv_dtype or pw.dtype,
                       "head_dim": pw.head_dim, "group": pw.num_q_heads // pw.num_kv_heads,
                       "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "tokens_per_s": round(pw.total_q / (ms * 1e-3), 1)}), flush=True)

@@ -56,6 +56,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
 
 // Packed fp32 pairs (sm_100 and later): two IEEE fp32 operations per instruction,
 // each rounded exactly as the scalar one.
+// Non-blocking look at an mbarrier phase (acquire, CTA scope): true once the
+// phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -137,38 +151,50 @@ struct PairLayout {
 // c ^ ((r >> 1) & 3) for 64-byte rows) are copied into the upper half of the
 // fp16 stage, and one warp widens them there to the fp16 tile the MMA reads
 // (128-byte rows of 64 dims per atom, unit k of row r at k ^ (r & 7)); every
-// code is exact in fp16.  Each pass reads 1 KB of codes into registers
-// before it writes: at head_dim 128 the codes of row r share their 128 bytes
-// with row r of the second atom only, and at head_dim 64 a pass writes over
-// codes of that pass or of earlier ones only, so nothing is overwritten
-// before it is read.
+// code is exact in fp16.  A pass covers 1 KB of codes (8 rows at head_dim
+// 128, 16 at 64); the warp reads kGroup passes into registers, then writes
+// them.  At head_dim 128 the codes of row r share their 128 bytes with row r
+// of the second atom only, and at head_dim 64 a group writes over codes of
+// that group or of earlier ones only, so nothing is overwritten before it is
+// read.
 template <int D>
 __device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
   constexpr int kRows = 1024 / D;      // rows per pass: 8 (d 128) or 16 (d 64)
   constexpr int kPerRow = 32 / kRows;  // lanes per row: 4 or 2
+  constexpr int kPasses = kPairKeys / kRows;
+  constexpr int kGroup = 4;            // passes read before the writes
+  static_assert(kPasses % kGroup == 0, "whole groups");
   const uint8_t *codes = st + (D / 64) * kPairKvAtom / 2;
+  const int c0 = 2 * (lane % kPerRow);  // this lane's 16-dim units c0 and c0 + 1
 #pragma unroll 1
-  for (int j = 0; j < kPairKeys / kRows; ++j) {
-    const int r = j * kRows + lane / kPerRow;
-    const int c0 = 2 * (lane % kPerRow);  // this lane's 16-dim units c0 and c0 + 1
-    const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
-    const uint4 x0 = *reinterpret_cast<const uint4 *>(codes + r * D + ((c0 ^ sw) << 4));
-    const uint4 x1 = *reinterpret_cast<const uint4 *>(codes + r * D + (((c0 + 1) ^ sw) << 4));
+  for (int j0 = 0; j0 < kPasses; j0 += kGroup) {
+    uint4 x[kGroup][2];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const int r = (j0 + g) * kRows + lane / kPerRow;
+      const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
+      x[g][0] = *reinterpret_cast<const uint4 *>(codes + r * D + ((c0 ^ sw) << 4));
+      x[g][1] = *reinterpret_cast<const uint4 *>(codes + r * D + (((c0 + 1) ^ sw) << 4));
+    }
     __syncwarp();
-    uint32_t h0[8], h1[8];
-    e4m3x16_to_half(x0, h0);
-    e4m3x16_to_half(x1, h1);
-    // unit c (dims 16 c .. 16 c + 15) becomes fp16 units 2 (c & 3) and
-    // 2 (c & 3) + 1 of atom c / 4
-    uint8_t *row = st + (c0 >> 2) * kPairKvAtom + r * 128;
-    const int k0 = 2 * (c0 & 3);
-    *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-    *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ (r & 7)) << 4)) =
-        make_uint4(h0[4], h0[5], h0[6], h0[7]);
-    *reinterpret_cast<uint4 *>(row + (((k0 + 2) ^ (r & 7)) << 4)) =
-        make_uint4(h1[0], h1[1], h1[2], h1[3]);
-    *reinterpret_cast<uint4 *>(row + (((k0 + 3) ^ (r & 7)) << 4)) =
-        make_uint4(h1[4], h1[5], h1[6], h1[7]);
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const int r = (j0 + g) * kRows + lane / kPerRow;
+      uint32_t h0[8], h1[8];
+      e4m3x16_to_half(x[g][0], h0);
+      e4m3x16_to_half(x[g][1], h1);
+      // unit c (dims 16 c .. 16 c + 15) becomes fp16 units 2 (c & 3) and
+      // 2 (c & 3) + 1 of atom c / 4
+      uint8_t *row = st + (c0 >> 2) * kPairKvAtom + r * 128;
+      const int k0 = 2 * (c0 & 3), sw = r & 7;
+      *reinterpret_cast<uint4 *>(row + ((k0 ^ sw) << 4)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+      *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ sw) << 4)) =
+          make_uint4(h0[4], h0[5], h0[6], h0[7]);
+      *reinterpret_cast<uint4 *>(row + (((k0 + 2) ^ sw) << 4)) =
+          make_uint4(h1[0], h1[1], h1[2], h1[3]);
+      *reinterpret_cast<uint4 *>(row + (((k0 + 3) ^ sw) << 4)) =
+          make_uint4(h1[4], h1[5], h1[6], h1[7]);
+    }
     __syncwarp();
   }
 }
@@ -723,9 +749,12 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     bool ok_run = true;
     if constexpr (F8) {
       // A step's copies (16 rows of head_dim codes per sub-tile) land in the
-      // upper half of its stage; the warp widens a step to fp16 S - 1 steps
-      // after issuing its copies (so S - 1 steps of copies stay in flight),
-      // clears what V must not contribute, and hands the stage over.
+      // upper half of its stage; the warp widens them to fp16 there, clears
+      // what V must not contribute and hands the stage over.  Copies and
+      // widening each go ahead as soon as their own barrier allows (a stage
+      // released by the MMAs, a step's codes in), so the widening of step m
+      // waits for nothing later than the release of step m - S; the warp
+      // polls both and gives up after kWaitLimitNs without progress.
       constexpr int kF8Sub = 16 * D;                // bytes of one sub-tile's codes
       constexpr int kStage = kAtoms * kPairKvAtom;  // bytes of one fp16 stage
       const int S = k_role ? SK : SV;
@@ -734,65 +763,76 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       uint64_t *empty = k_role ? k_empty : v_empty;
       uint8_t *ring = smem + (k_role ? L::kKOff : L::kVOff);
       const CUtensorMap *map = k_role ? &kmap : &vmap;
-      for (int n = 0; n < n_steps + S - 1 && ok_run; ++n) {
-        if (n < n_steps) {
-          if (n * kSub >= win_base + 32) {
-            win_base += 32;
-            win = block_of(win_base + lane);
-          }
-          const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
-          const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
-          const int s = n % S;
-          if (lane == 0) {
-            if (n >= S && !mbar_wait_bounded(&empty[s], ((n / S) - 1) & 1)) {
-              ok_run = false;
-            } else {
+      int n_issue = 0, n_conv = 0;
+      uint64_t t_prog = global_timer_ns();
+      while (n_conv < n_steps) {
+        bool progressed = false;
+        if (n_issue < n_steps) {
+          const int n = n_issue, s = n % S;
+          bool free_stage = true;
+          if (lane == 0 && n >= S) free_stage = mbar_test_wait(&empty[s], ((n / S) - 1) & 1);
+          if (__shfl_sync(kFullMask, free_stage ? 1 : 0, 0)) {
+            if (n * kSub >= win_base + 32) {
+              win_base += 32;
+              win = block_of(win_base + lane);
+            }
+            const int my_phys =
+                __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
+            const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
+            if (lane == 0) {
               if (!k_role) v_masks[s] = mask;
               if (mask == 0)
                 mbar_arrive(&land[s]);
               else
                 mbar_arrive_expect_tx(&land[s], __popc(mask) * kF8Sub);
             }
-          }
-          ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
-          if (!ok_run) break;
-          __syncwarp();
-          if (lane < kSub && my_phys >= 0) {
-            const int u = n * kSub + lane;
-            const int y =
-                ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((key_base + u * 16) & bs_mask);
-            tma_load_2d(ring + s * kStage + kStage / 2 + lane * kF8Sub, map, 0, y, &land[s],
-                        policy);
-          }
-        }
-        const int m = n - (S - 1);
-        if (m < 0) continue;
-        const int s = m % S;
-        bool got = true;
-        if (lane == 0) got = mbar_wait_bounded(&land[s], (m / S) & 1);
-        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
-        if (!got) {
-          ok_run = false;
-          break;
-        }
-        uint8_t *st = ring + s * kStage;
-        f8_stage_to_f16<D>(st, lane);
-        if (!k_role) {
-          // V rows past n_keys and of sub-tiles not loaded become zeros
-          const uint32_t vm = v_masks[s];
-          const int first = n_keys - m * kPairKeys;  // first row to clear
-          if (vm != kAllSub || first < kPairKeys) {
-            for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {  // 16-byte units
-              const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
-              if (row >= first || !((vm >> (row >> 4)) & 1u))
-                *reinterpret_cast<uint4 *>(st + b * kPairKvAtom + row * 128 + u16 * 16) =
-                    make_uint4(0, 0, 0, 0);
+            __syncwarp();
+            if (lane < kSub && my_phys >= 0) {
+              const int u = n * kSub + lane;
+              const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) +
+                            ((key_base + u * 16) & bs_mask);
+              tma_load_2d(ring + s * kStage + kStage / 2 + lane * kF8Sub, map, 0, y, &land[s],
+                          policy);
             }
+            ++n_issue;
+            progressed = true;
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (n_conv < n_issue) {
+          const int m = n_conv, s = m % S;
+          // every lane observes the copies' completion before it reads them
+          if (__all_sync(kFullMask, mbar_test_wait(&land[s], (m / S) & 1))) {
+            uint8_t *st = ring + s * kStage;
+            f8_stage_to_f16<D>(st, lane);
+            if (!k_role) {
+              // V rows past n_keys and of sub-tiles not loaded become zeros
+              const uint32_t vm = v_masks[s];
+              const int first = n_keys - m * kPairKeys;  // first row to clear
+              if (vm != kAllSub || first < kPairKeys) {
+                for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {  // 16-byte units
+                  const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
+                  if (row >= first || !((vm >> (row >> 4)) & 1u))
+                    *reinterpret_cast<uint4 *>(st + b * kPairKvAtom + row * 128 + u16 * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
+            ++n_conv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_prog = global_timer_ns();
+        } else {
+          if (global_timer_ns() - t_prog > kWaitLimitNs) {
+            ok_run = false;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
     } else {
     for (int n = 0; n < n_steps && ok_run; ++n) {
