@@ -177,22 +177,27 @@ __device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
       x[g][1] = *reinterpret_cast<const uint4 *>(codes + r * D + (((c0 + 1) ^ sw) << 4));
     }
     __syncwarp();
+    // At head_dim 128 the lanes of the second atom take their units in the
+    // other order, so the eight lanes of each store phase (two rows, four
+    // lanes each) write eight different 16-byte bank groups.
+    const bool flip = D == 128 && (lane & 2);
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       const int r = (j0 + g) * kRows + lane / kPerRow;
+      const uint4 xa = flip ? x[g][1] : x[g][0], xb = flip ? x[g][0] : x[g][1];
       uint32_t h0[8], h1[8];
-      e4m3x16_to_half(x[g][0], h0);
-      e4m3x16_to_half(x[g][1], h1);
+      e4m3x16_to_half(xa, h0);
+      e4m3x16_to_half(xb, h1);
       // unit c (dims 16 c .. 16 c + 15) becomes fp16 units 2 (c & 3) and
-      // 2 (c & 3) + 1 of atom c / 4
+      // 2 (c & 3) + 1 of atom c / 4; h0 holds unit c0 + flip, h1 the other
       uint8_t *row = st + (c0 >> 2) * kPairKvAtom + r * 128;
-      const int k0 = 2 * (c0 & 3), sw = r & 7;
-      *reinterpret_cast<uint4 *>(row + ((k0 ^ sw) << 4)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-      *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ sw) << 4)) =
+      const int ka = 2 * (c0 & 3) + (flip ? 2 : 0), kb = 2 * (c0 & 3) + (flip ? 0 : 2);
+      const int sw = r & 7;
+      *reinterpret_cast<uint4 *>(row + ((ka ^ sw) << 4)) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+      *reinterpret_cast<uint4 *>(row + (((ka + 1) ^ sw) << 4)) =
           make_uint4(h0[4], h0[5], h0[6], h0[7]);
-      *reinterpret_cast<uint4 *>(row + (((k0 + 2) ^ sw) << 4)) =
-          make_uint4(h1[0], h1[1], h1[2], h1[3]);
-      *reinterpret_cast<uint4 *>(row + (((k0 + 3) ^ sw) << 4)) =
+      *reinterpret_cast<uint4 *>(row + ((kb ^ sw) << 4)) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+      *reinterpret_cast<uint4 *>(row + (((kb + 1) ^ sw) << 4)) =
           make_uint4(h1[4], h1[5], h1[6], h1[7]);
     }
     __syncwarp();
