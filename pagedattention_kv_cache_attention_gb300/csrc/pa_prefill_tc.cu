@@ -131,8 +131,13 @@ constexpr int kPairKvAtom = kPairKeys * 128;   // one 64-dim atom of a K or V st
 
 // TILES query tiles per CTA: softmax warps 0 .. 4 TILES - 1, issuing warps
 // 4 TILES .. 6 TILES - 1 (Q K^T and P V of each tile), then the K and V warps.
-template <int TILES>
-constexpr int pair_threads() { return 32 * (6 * TILES + 2); }
+// Over FP8 caches at head_dim 128 the two-tile kernel has two more warps that
+// widen half of each step's K and V codes, so the widening is spread over all
+// four schedulers of the SM.
+template <int TILES, int D = 128, bool F8 = false>
+__host__ __device__ constexpr bool f8_helpers() { return F8 && TILES == 2 && D == 128; }
+template <int TILES, int D = 128, bool F8 = false>
+constexpr int pair_threads() { return 32 * (6 * TILES + 2 + (f8_helpers<TILES, D, F8>() ? 2 : 0)); }
 
 template <int SK, int SV, int TILES, int D>
 struct PairLayout {
@@ -152,13 +157,14 @@ struct PairLayout {
 // fp16 stage, and one warp widens them there to the fp16 tile the MMA reads
 // (128-byte rows of 64 dims per atom, unit k of row r at k ^ (r & 7)); every
 // code is exact in fp16.  A pass covers 1 KB of codes (8 rows at head_dim
-// 128, 16 at 64); the warp reads kGroup passes into registers, then writes
-// them.  At head_dim 128 the codes of row r share their 128 bytes with row r
+// 128, 16 at 64); the warp widens passes [pass_begin, pass_end) (whole groups),
+// reading kGroup passes into registers before it writes them.  At head_dim 128 the codes of row r share their 128 bytes with row r
 // of the second atom only, and at head_dim 64 a group writes over codes of
 // that group or of earlier ones only, so nothing is overwritten before it is
 // read.
 template <int D>
-__device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
+__device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane, int pass_begin,
+                                                int pass_end) {
   constexpr int kRows = 1024 / D;      // rows per pass: 8 (d 128) or 16 (d 64)
   constexpr int kPerRow = 32 / kRows;  // lanes per row: 4 or 2
   constexpr int kPasses = kPairKeys / kRows;
@@ -167,7 +173,7 @@ __device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
   const uint8_t *codes = st + (D / 64) * kPairKvAtom / 2;
   const int c0 = 2 * (lane % kPerRow);  // this lane's 16-dim units c0 and c0 + 1
 #pragma unroll 1
-  for (int j0 = 0; j0 < kPasses; j0 += kGroup) {
+  for (int j0 = pass_begin; j0 < pass_end; j0 += kGroup) {
     uint4 x[kGroup][2];
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
@@ -208,7 +214,7 @@ __device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane) {
 // products then run in fp16 whatever T is (bf16 queries are carried in fp16,
 // see the Q load).
 template <typename T, int D, int SK, int SV, bool SPLIT, int TILES, bool PX, bool F8>
-__global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
+__global__ void __launch_bounds__(pair_threads<TILES, D, F8>(), TILES == 1 ? 2 : 1)
     pa_prefill_tc_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                               const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
@@ -219,6 +225,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
   constexpr int kAtoms = L::kAtoms;
   constexpr int kIssue0 = 4 * TILES;      // first MMA-issuing warp
   constexpr int kLoad0 = 6 * TILES;       // K producer warp (V: kLoad0 + 1)
+  // FP8 widening helpers (K: kLoad0 + 2, V: kLoad0 + 3); a stage is handed
+  // over by every warp that widens part of it
+  constexpr bool kHelpers = f8_helpers<TILES, D, F8>();
+  constexpr int kWideners = kHelpers ? 2 : 1;
   constexpr int kSub = kPairKeys / 16;         // 16-row sub-tiles per step
   constexpr uint32_t kAllSub = (1u << kSub) - 1;
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
@@ -260,11 +270,11 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
 
   if (tid == 0) {
     for (int s = 0; s < SK; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], F8 ? kWideners : 1);
       mbar_init(&k_empty[s], TILES);  // released by every Q K^T issuer
     }
     for (int s = 0; s < SV; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], F8 ? kWideners : 1);
       mbar_init(&v_empty[s], TILES);  // and every P V issuer
     }
     mbar_init(v_tail, 1);
@@ -737,7 +747,10 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     }
   } else if (active && warp >= kLoad0) {
     // ---------------------------------------------------- TMA producers (K, V)
-    const bool k_role = warp == kLoad0;
+    // (and, over FP8 caches at head_dim 128 with two tiles, the K and V
+    // widening helpers)
+    const bool k_role = ((warp - kLoad0) & 1) == 0;
+    const bool helper = warp - kLoad0 >= 2;
     const int bs_mask = (1 << a.bs_log2) - 1;
     auto block_of = [&](int u) -> int {
       if (u >= n_sub) return -1;
@@ -750,7 +763,7 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
     };
     const uint64_t policy = l2_policy_evict_first();
     int win_base = 0;
-    int win = block_of(lane);
+    int win = helper ? -1 : block_of(lane);
     bool ok_run = true;
     if constexpr (F8) {
       // A step's copies (16 rows of head_dim codes per sub-tile) land in the
@@ -762,81 +775,104 @@ __global__ void __launch_bounds__(pair_threads<TILES>(), TILES == 1 ? 2 : 1)
       // polls both and gives up after kWaitLimitNs without progress.
       constexpr int kF8Sub = 16 * D;                // bytes of one sub-tile's codes
       constexpr int kStage = kAtoms * kPairKvAtom;  // bytes of one fp16 stage
+      constexpr int kPassRows = 1024 / D;           // rows per 1 KB pass of codes
+      constexpr int kPasses = kPairKeys / kPassRows;
       const int S = k_role ? SK : SV;
       uint64_t *land = k_role ? k_land : v_land;
       uint64_t *full = k_role ? k_full : v_full;
       uint64_t *empty = k_role ? k_empty : v_empty;
       uint8_t *ring = smem + (k_role ? L::kKOff : L::kVOff);
       const CUtensorMap *map = k_role ? &kmap : &vmap;
-      int n_issue = 0, n_conv = 0;
-      uint64_t t_prog = global_timer_ns();
-      while (n_conv < n_steps) {
-        bool progressed = false;
-        if (n_issue < n_steps) {
-          const int n = n_issue, s = n % S;
-          bool free_stage = true;
-          if (lane == 0 && n >= S) free_stage = mbar_test_wait(&empty[s], ((n / S) - 1) & 1);
-          if (__shfl_sync(kFullMask, free_stage ? 1 : 0, 0)) {
-            if (n * kSub >= win_base + 32) {
-              win_base += 32;
-              win = block_of(win_base + lane);
+      // this warp's passes of every step: all of them, or with helpers the
+      // first half (producer) or the second (helper)
+      const int pass0 = kHelpers && helper ? kPasses / 2 : 0;
+      const int pass1 = kHelpers && !helper ? kPasses / 2 : kPasses;
+      // widen this warp's passes of step m (its codes are in), clear the V
+      // rows among them that must not contribute, and hand the stage over
+      auto widen = [&](int m) {
+        const int s = m % S;
+        uint8_t *st = ring + s * kStage;
+        f8_stage_to_f16<D>(st, lane, pass0, pass1);
+        if (!k_role) {
+          // V rows past n_keys and of sub-tiles not loaded become zeros
+          const uint32_t vm = v_masks[s];
+          const int first = n_keys - m * kPairKeys;  // first row to clear
+          if (vm != kAllSub || first < kPairKeys) {
+            const int row0 = pass0 * kPassRows;
+            for (int i = lane; i < (pass1 - pass0) * kPassRows * kAtoms * 8; i += 32) {
+              const int row = row0 + i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
+              if (row >= first || !((vm >> (row >> 4)) & 1u))
+                *reinterpret_cast<uint4 *>(st + b * kPairKvAtom + row * 128 + u16 * 16) =
+                    make_uint4(0, 0, 0, 0);
             }
-            const int my_phys =
-                __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
-            const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
-            if (lane == 0) {
-              if (!k_role) v_masks[s] = mask;
-              if (mask == 0)
-                mbar_arrive(&land[s]);
-              else
-                mbar_arrive_expect_tx(&land[s], __popc(mask) * kF8Sub);
-            }
-            __syncwarp();
-            if (lane < kSub && my_phys >= 0) {
-              const int u = n * kSub + lane;
-              const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) +
-                            ((key_base + u * 16) & bs_mask);
-              tma_load_2d(ring + s * kStage + kStage / 2 + lane * kF8Sub, map, 0, y, &land[s],
-                          policy);
-            }
-            ++n_issue;
-            progressed = true;
           }
         }
-        if (n_conv < n_issue) {
-          const int m = n_conv, s = m % S;
-          // every lane observes the copies' completion before it reads them
-          if (__all_sync(kFullMask, mbar_test_wait(&land[s], (m / S) & 1))) {
-            uint8_t *st = ring + s * kStage;
-            f8_stage_to_f16<D>(st, lane);
-            if (!k_role) {
-              // V rows past n_keys and of sub-tiles not loaded become zeros
-              const uint32_t vm = v_masks[s];
-              const int first = n_keys - m * kPairKeys;  // first row to clear
-              if (vm != kAllSub || first < kPairKeys) {
-                for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {  // 16-byte units
-                  const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
-                  if (row >= first || !((vm >> (row >> 4)) & 1u))
-                    *reinterpret_cast<uint4 *>(st + b * kPairKvAtom + row * 128 + u16 * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
-            ++n_conv;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_prog = global_timer_ns();
-        } else {
-          if (global_timer_ns() - t_prog > kWaitLimitNs) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      };
+      if (helper) {
+        // every step in order, once its codes are in (each lane observes it)
+        for (int m = 0; m < n_steps; ++m) {
+          if (!__all_sync(kFullMask, mbar_wait_bounded(&land[m % S], (m / S) & 1))) {
             ok_run = false;
             break;
           }
-          __nanosleep(32);
+          widen(m);
+        }
+      } else {
+        int n_issue = 0, n_conv = 0;
+        uint64_t t_prog = global_timer_ns();
+        while (n_conv < n_steps) {
+          bool progressed = false;
+          if (n_issue < n_steps) {
+            const int n = n_issue, s = n % S;
+            bool free_stage = true;
+            if (lane == 0 && n >= S) free_stage = mbar_test_wait(&empty[s], ((n / S) - 1) & 1);
+            if (__shfl_sync(kFullMask, free_stage ? 1 : 0, 0)) {
+              if (n * kSub >= win_base + 32) {
+                win_base += 32;
+                win = block_of(win_base + lane);
+              }
+              const int my_phys =
+                  __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
+              const uint32_t mask =
+                  __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
+              if (lane == 0) {
+                if (!k_role) v_masks[s] = mask;
+                if (mask == 0)
+                  mbar_arrive(&land[s]);
+                else
+                  mbar_arrive_expect_tx(&land[s], __popc(mask) * kF8Sub);
+              }
+              __syncwarp();
+              if (lane < kSub && my_phys >= 0) {
+                const int u = n * kSub + lane;
+                const int y = ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) +
+                              ((key_base + u * 16) & bs_mask);
+                tma_load_2d(ring + s * kStage + kStage / 2 + lane * kF8Sub, map, 0, y, &land[s],
+                            policy);
+              }
+              ++n_issue;
+              progressed = true;
+            }
+          }
+          // every lane observes the copies' completion before it reads them
+          if (n_conv < n_issue &&
+              __all_sync(kFullMask, mbar_test_wait(&land[n_conv % S], (n_conv / S) & 1))) {
+            widen(n_conv);
+            ++n_conv;
+            progressed = true;
+          }
+          if (progressed) {
+            t_prog = global_timer_ns();
+          } else {
+            if (global_timer_ns() - t_prog > kWaitLimitNs) {
+              ok_run = false;
+              break;
+            }
+            __nanosleep(32);
+          }
         }
       }
     } else {
@@ -966,11 +1002,12 @@ cudaError_t launch_prefill_tc_pair_t(const PrefillArgs &a, const CUtensorMap &km
         kern,
         dim3(static_cast<unsigned>(a.num_parts * a.chunks), static_cast<unsigned>(a.num_kv_heads),
              static_cast<unsigned>(a.num_groups)),
-        dim3(pair_threads<TILES>()), smem, stream, km, vm, a);
+        dim3(pair_threads<TILES, D, F8>()), smem, stream, km, vm, a);
   }
   const int tpc = TILES * kTcRows / a.group;
   const int tiles = (a.max_q_len + tpc - 1) / tpc;
-  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs), dim3(pair_threads<TILES>()), smem,
+  return launch_dependent(kern, dim3(tiles, a.num_kv_heads, a.num_seqs),
+                          dim3(pair_threads<TILES, D, F8>()), smem,
                           stream, km, vm, a);
 }
 
