@@ -220,7 +220,8 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
  *               the call is pa_decode.
  * Other arguments, the workspace (pa_decode_workspace_size bytes, counter
  * words zero) and the accuracy are as for pa_decode; dtype fp16 or bf16
- * caches.  Input errors only the device can see set PA_DEVERR_PREFIX (see
+ * caches (FP8 caches: pa_decode_shared_prefix_fp8 below).  Input errors only
+ * the device can see set PA_DEVERR_PREFIX (see
  * above): the output of the sequences concerned is then unspecified, never a
  * fault.
  */

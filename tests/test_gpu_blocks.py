@@ -113,7 +113,12 @@ def test_fork_then_write_leaves_sharer_unchanged(pa):
     others = [i for i in range(w.num_seqs) if i != 1]
     assert torch.equal(after2[others].view(torch.int16), before[others].view(torch.int16))
     assert not torch.equal(after2[1].view(torch.int16), before[1].view(torch.int16))
-    kh, vh = u16(kc), u16(vc)
+    # the oracle's own pools through the same steps: scatter, fork, write
+    kh, vh = u16(w.k_cache).copy(), u16(w.v_cache).copy()
+    oracle.reshape_and_cache(w.key, w.value, kh, vh, w.slot_mapping)
+    oracle.copy_blocks(kh, vh, m.numpy())
+    oracle.reshape_and_cache(key, key, kh, vh, slot)
+    assert np.array_equal(u16(kc), kh) and np.array_equal(u16(vc), vh)
     ref = oracle.decode(w.query, kh, vh, bt, w.context_lens, w.scale, w.dtype,
                         pairs=[(1, h) for h in range(w.num_q_heads)])
     got = after2[1].float().cpu().double().numpy()
@@ -135,19 +140,22 @@ def test_swap_out_and_back_in(pa, dtype):
     victims = [(i, lb) for i in range(4) for lb in range(int(nblk[i]))]
     dev_ids = np.array([int(w.block_tables[i, lb]) for i, lb in victims], np.int64)
     n = len(victims)
-    host_k = torch.empty((n + 5,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
-    host_v = torch.empty_like(host_k).pin_memory()
+    host_k = torch.zeros((n + 5,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+    host_v = torch.zeros_like(host_k).pin_memory()
     out_map = torch.from_numpy(np.stack([dev_ids, np.arange(n) + 5], 1)).pin_memory()
     pa.pa_swap_blocks(kc, host_k, out_map)
     pa.pa_swap_blocks(vc, host_v, out_map)
     torch.cuda.synchronize()
     assert pa.pa_device_errors() == 0
-    # host pool bit-exact against the oracle's swap of the same blocks
-    hk = np.zeros((n + 5,) + tuple(kc.shape[1:]), np.uint16)
-    hk[:] = u16(host_k)[:]
-    exp = u16(host_k).copy()
-    oracle.swap_blocks(u16(kc), exp, out_map.numpy())
-    assert np.array_equal(hk, exp)
+    # host pool bit-exact against the oracle's swap of the same blocks out of
+    # the oracle's own pool (after its scatter) into a zeroed pool
+    kh = u16(w.k_cache).copy()
+    vh = u16(w.v_cache).copy()
+    oracle.reshape_and_cache(w.key, w.value, kh, vh, w.slot_mapping)
+    assert np.array_equal(u16(kc), kh)
+    exp = np.zeros((n + 5,) + tuple(kc.shape[1:]), np.uint16)
+    oracle.swap_blocks(kh, exp, out_map.numpy())
+    assert np.array_equal(u16(host_k), exp)
     # the freed device blocks get reused (garbage), the victims come back elsewhere
     kc[torch.from_numpy(dev_ids).to(dev)] = float("nan")
     vc[torch.from_numpy(dev_ids).to(dev)] = float("nan")

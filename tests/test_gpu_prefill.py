@@ -36,9 +36,21 @@ def run(pa, pw):
     return kc, vc, out, pa.pa_device_errors()
 
 
+def host_pool(pw):
+    """The oracle's pools after its own scatter of the chunk tokens."""
+    kh = pw.k_cache.view(torch.int16).numpy().view(np.uint16).copy()
+    vh = pw.v_cache.view(torch.int16).numpy().view(np.uint16).copy()
+    oracle.reshape_and_cache(pw.key, pw.value, kh, vh, pw.slot_mapping)
+    return kh, vh
+
+
+def gpu_u16(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
 def check(pw, kc, vc, out, rows=None):
-    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
-    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    kh, vh = host_pool(pw)
+    assert np.array_equal(gpu_u16(kc), kh) and np.array_equal(gpu_u16(vc), vh)
     ref = oracle.prefill(pw.query, pw.query_start, kh, vh, pw.block_tables, pw.context_lens,
                          pw.scale, pw.dtype)
     got = out.float().cpu().double().numpy()
@@ -128,8 +140,8 @@ def test_prefill_bench_size_repeatable(pa, dtype):
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
     # the oracle on four whole sequences of the launch (each sequence is independent)
-    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
-    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    kh, vh = host_pool(pw)
+    assert np.array_equal(gpu_u16(kc), kh) and np.array_equal(gpu_u16(vc), vh)
     qs_h = pw.query_start.numpy()
     for i in (0, 21, 42, 63):
         a, b = int(qs_h[i]), int(qs_h[i + 1])
@@ -161,8 +173,8 @@ def test_prefill_bad_block_flagged_others_exact(pa, chunk, head_dim):
     qs_h = pw.query_start.numpy()
     a1, b1 = int(qs_h[1]), int(qs_h[2])
     assert torch.isfinite(out[a1:b1].float()).all()
-    kh = kc.cpu().view(torch.int16).numpy().view(np.uint16)
-    vh = vc.cpu().view(torch.int16).numpy().view(np.uint16)
+    kh, vh = host_pool(pw)
+    assert np.array_equal(gpu_u16(kc), kh) and np.array_equal(gpu_u16(vc), vh)
     for i in (0, 2):
         a, b = int(qs_h[i]), int(qs_h[i + 1])
         ref = oracle.prefill(pw.query[a:b], np.array([0, b - a], dtype=np.int32), kh, vh,
