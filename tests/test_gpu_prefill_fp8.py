@@ -123,3 +123,39 @@ def test_prefill_fp8_random_shapes(pa, i):
     kc, vc, out, err = run(pa, pw)
     assert err == 0
     check(pw, kc, vc, out)
+
+
+@pytest.mark.parametrize("chunk,head_dim", [(300, 128), (20, 128), (40, 64), (10, 64)],
+                         ids=["two-tile", "one-tile", "two-tile-d64", "one-tile-d64"])
+def test_prefill_fp8_bad_block_flagged_others_exact(pa, chunk, head_dim):
+    """An out-of-range block id in one sequence's table: the call flags it,
+    reads nothing through it (the sub-tile's codes are never copied, its V rows
+    are cleared after the widening, so that sequence's rows stay finite), and
+    every other sequence's rows still match the oracle."""
+    pw = W.to_fp8(W.make_prefill("llama3_8b_gqa", 85, lens=[700, 1400, 900], chunk=chunk,
+                                 head_dim=head_dim))
+    dev = torch.device("cuda")
+    kc, vc = pw.k_cache.to(dev), pw.v_cache.to(dev)
+    pa.pa_reshape_and_cache_fp8(pw.key.to(dev), pw.value.to(dev), kc, vc,
+                                pw.slot_mapping.to(dev), pw.k_scale, pw.v_scale)
+    bt = pw.block_tables.clone()
+    bt[1, 5] = pw.num_blocks + 7          # a block well inside sequence 1's context
+    q, qs = pw.query.to(dev), pw.query_start.to(dev)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_prefill_fp8(out, q, qs, kc, vc, bt.to(dev), pw.context_lens.to(dev), pw.scale,
+                      pw.k_scale, pw.v_scale, pw.max_q_len)
+    torch.cuda.synchronize()
+    assert pa.pa_device_errors() & pa.DEVERR_BAD_BLOCK
+    qs_h = pw.query_start.numpy()
+    a1, b1 = int(qs_h[1]), int(qs_h[2])
+    assert torch.isfinite(out[a1:b1].float()).all()
+    kh, vh = host_pool(pw)
+    assert np.array_equal(kc.cpu().numpy(), kh) and np.array_equal(vc.cpu().numpy(), vh)
+    for i in (0, 2):
+        a, b = int(qs_h[i]), int(qs_h[i + 1])
+        ref = oracle.prefill(pw.query[a:b], np.array([0, b - a], dtype=np.int32), kh, vh,
+                             pw.block_tables[i:i + 1], pw.context_lens[i:i + 1], pw.scale,
+                             pw.dtype, kv_dtype="e4m3", k_scale=pw.k_scale, v_scale=pw.v_scale)
+        got = out[a:b].float().cpu().double().numpy()
+        err = np.abs(got - ref)
+        assert not (err > ATOL + RTOL * np.abs(ref)).any(), f"seq {i}: max err {err.max():.3g}"
