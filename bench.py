@@ -46,7 +46,7 @@ MODEL_LAYERS = {"llama3_8b_gqa": 32, "shared_prefix_cow": 32, "long_context": 32
 DEFAULT_WORKLOAD = "llama3_70b_cb"
 # the other decode targets measured beside the default line, in the same run
 DEFAULT_EXTRAS = ("llama3_8b_gqa:fp16", "llama3_70b_cb:bf16", "shared_prefix_cow:shared",
-                  "shared_prefix_cow")
+                  "shared_prefix_cow", "llama3_70b_cb:e4m3", "llama3_8b_gqa:e4m3")
 DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh", "pa_tile.cuh")
 
 
@@ -460,8 +460,10 @@ def time_each(fn, K: int, stream, dev) -> float:
 
 
 def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
-    """Step and decode-call figures of another workload ("name:dtype"), in the
-    same run and on the same stream as the main line."""
+    """Step and decode-call figures of another workload ("name:flag:..." with
+    flags fp16 / bf16 for the query and cache type, e4m3 for FP8 caches,
+    shared for the shared-prefix call), in the same run and on the same stream
+    as the main line."""
     import torch
 
     import workloads
@@ -469,6 +471,8 @@ def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
     dtype = next((f for f in flags if f in ("fp16", "bf16")), None)
     shared = "shared" in flags
     w = workloads.make(name, seed=args.seed, **({"dtype": dtype} if dtype else {}))
+    if "e4m3" in flags:
+        w = workloads.to_fp8(w)
     ab = algorithmic_bytes(w)
     s = Step(pa, w, dev, shared=shared)
     for _ in range(args.warmup):
@@ -479,7 +483,8 @@ def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
     if pa.pa_device_errors(stream) != 0:
         raise RuntimeError(f"device error bits raised on {spec}")
     dec_gbs = ab["decode"] / (dms * 1e-3) / 1e9
-    res = {"workload": w.name, "dtype": w.dtype, "batch": w.num_seqs,
+    res = {"workload": w.name, "dtype": w.dtype, "kv_dtype": w.kv_dtype or w.dtype,
+           "batch": w.num_seqs,
            "partition_size": w.partition_size, "partitions": s.nparts,
            "ms_per_step": round(ms, 5),
            "value": round(ab["step"] / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -490,7 +495,8 @@ def measure_extra(pa, spec: str, args, dev, stream, peak: float) -> dict:
            "gpu_launches_per_step": s.launches_per_step()}
     if "kv_unique" in ab:
         # bytes of distinct slots (a shared prefix counted once per group)
-        res["decode"] = "pa_decode_shared_prefix" if shared else "pa_decode"
+        res["decode"] = (("pa_decode_shared_prefix" if shared else "pa_decode")
+                         + ("_fp8" if s.fp8 else ""))
         res["unique"] = {"step_gbs": round(ab["step_unique"] / (ms * 1e-3) / 1e9, 2),
                          "hbm_fraction": round(ab["step_unique"] / (ms * 1e-3) / 1e9 / peak, 4),
                          "decode_gbs": round(ab["decode_unique"] / (dms * 1e-3) / 1e9, 2),
