@@ -154,14 +154,14 @@ struct PairLayout {
 // FP8 E4M3 caches: a step's codes (64 rows of D bytes, in the pool map's
 // swizzle: 16-byte unit c of row r at unit c ^ (r & 7) for 128-byte rows,
 // c ^ ((r >> 1) & 3) for 64-byte rows) are copied into the upper half of the
-// fp16 stage, and one warp widens them there to the fp16 tile the MMA reads
-// (128-byte rows of 64 dims per atom, unit k of row r at k ^ (r & 7)); every
-// code is exact in fp16.  A pass covers 1 KB of codes (8 rows at head_dim
-// 128, 16 at 64); the warp widens passes [pass_begin, pass_end) (whole groups),
-// reading kGroup passes into registers before it writes them.  At head_dim 128 the codes of row r share their 128 bytes with row r
-// of the second atom only, and at head_dim 64 a group writes over codes of
-// that group or of earlier ones only, so nothing is overwritten before it is
-// read.
+// fp16 stage and widened there to the fp16 tile the MMA reads (128-byte rows
+// of 64 dims per atom, unit k of row r at k ^ (r & 7)); every code is exact
+// in fp16.  A pass covers 1 KB of codes (8 rows at head_dim 128, 16 at 64);
+// a warp widens passes [pass_begin, pass_end) (whole groups), reading kGroup
+// passes into registers before it writes them.  At head_dim 128 the codes of
+// row r share their 128 bytes with row r of the second atom only, and at
+// head_dim 64 a group writes over codes of that group or of earlier ones
+// only, so nothing is overwritten before it is read.
 template <int D>
 __device__ __forceinline__ void f8_stage_to_f16(uint8_t *st, int lane, int pass_begin,
                                                 int pass_end) {
@@ -876,99 +876,99 @@ __global__ void __launch_bounds__(pair_threads<TILES, D, F8>(), TILES == 1 ? 2 :
         }
       }
     } else {
-    for (int n = 0; n < n_steps && ok_run; ++n) {
-      if (n * kSub >= win_base + 32) {
-        win_base += 32;
-        win = block_of(win_base + lane);
-      }
-      // lane h < kSub issues the copies of sub-tile h
-      const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
-      const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
-      const uint32_t bytes = __popc(mask) * kAtoms * 2048;
-      auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
-        if (lane < kSub && my_phys >= 0) {
-          const int u = n * kSub + lane;
-          const int y =
-              ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((key_base + u * 16) & bs_mask);
-#pragma unroll
-          for (int b = 0; b < kAtoms; ++b)
-            tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
+      for (int n = 0; n < n_steps && ok_run; ++n) {
+        if (n * kSub >= win_base + 32) {
+          win_base += 32;
+          win = block_of(win_base + lane);
         }
-      };
-      if (k_role) {
-        // the expected bytes are posted (lane 0) before any lane issues a copy
-        const int sk = n % SK;
-        if (lane == 0) {
-          if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
-            ok_run = false;
-          } else if (bytes == 0) {
-            mbar_arrive(&k_full[sk]);
-          } else {
-            mbar_arrive_expect_tx(&k_full[sk], bytes);
+        // lane h < kSub issues the copies of sub-tile h
+        const int my_phys = __shfl_sync(kFullMask, win, n * kSub + (lane & (kSub - 1)) - win_base);
+        const uint32_t mask = __ballot_sync(kFullMask, lane < kSub && my_phys >= 0) & kAllSub;
+        const uint32_t bytes = __popc(mask) * kAtoms * 2048;
+        auto load = [&](uint8_t *st, const CUtensorMap *map, uint64_t *bar) {
+          if (lane < kSub && my_phys >= 0) {
+            const int u = n * kSub + lane;
+            const int y =
+                ((my_phys * a.num_kv_heads + kvh) << a.bs_log2) + ((key_base + u * 16) & bs_mask);
+  #pragma unroll
+            for (int b = 0; b < kAtoms; ++b)
+              tma_load_2d(st + b * kPairKvAtom + lane * 2048, map, b * 64, y, bar, policy);
           }
+        };
+        if (k_role) {
+          // the expected bytes are posted (lane 0) before any lane issues a copy
+          const int sk = n % SK;
+          if (lane == 0) {
+            if (n >= SK && !mbar_wait_bounded(&k_empty[sk], ((n / SK) - 1) & 1)) {
+              ok_run = false;
+            } else if (bytes == 0) {
+              mbar_arrive(&k_full[sk]);
+            } else {
+              mbar_arrive_expect_tx(&k_full[sk], bytes);
+            }
+          }
+          ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
+          if (!ok_run) break;
+          __syncwarp();
+          load(smem + L::kKOff + sk * kAtoms * kPairKvAtom, &kmap, &k_full[sk]);
+          continue;
         }
+        // V: rows past the keys in use and sub-tiles not loaded become zeros
+        const int sv = n % SV;
+        uint8_t *vst = smem + L::kVOff + sv * kAtoms * kPairKvAtom;
+        if (lane == 0 && n >= SV && !mbar_wait_bounded(&v_empty[sv], ((n / SV) - 1) & 1))
+          ok_run = false;
         ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
         if (!ok_run) break;
         __syncwarp();
-        load(smem + L::kKOff + sk * kAtoms * kPairKvAtom, &kmap, &k_full[sk]);
-        continue;
+        const int key0 = n * kPairKeys;
+        const bool tail = key0 + kPairKeys > n_keys;
+        if (mask != kAllSub) {
+          // sub-tiles with no load: zero every 64-dim atom of their 16 rows
+          for (int i = lane; i < kSub * kAtoms * 16 * 8; i += 32) {  // 16-byte units
+            const int h = i / (kAtoms * 128), b = (i >> 7) % kAtoms, row = (i >> 3) & 15,
+                      u16 = i & 7;
+            if (!((mask >> h) & 1u))
+              *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + (h * 16 + row) * 128 + u16 * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (!tail) {
+          if (lane == 0) {
+            if (bytes == 0)
+              mbar_arrive(&v_full[sv]);
+            else
+              mbar_arrive_expect_tx(&v_full[sv], bytes);
+          }
+          __syncwarp();
+          load(vst, &vmap, &v_full[sv]);
+        } else {
+          // the last step: load, wait, zero the rows past n_keys, then hand over
+          if (lane == 0 && bytes > 0) mbar_arrive_expect_tx(v_tail, bytes);
+          __syncwarp();
+          load(vst, &vmap, v_tail);
+          bool got = true;
+          if (lane == 0 && bytes > 0) got = mbar_wait_bounded(v_tail, 0);
+          got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+          if (!got) {
+            ok_run = false;
+            break;
+          }
+          __syncwarp();
+          const int first = n_keys - key0;  // first row to clear
+          for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {
+            const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
+            if (row >= first)
+              *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + row * 128 + u16 * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&v_full[sv]);
+        }
       }
-      // V: rows past the keys in use and sub-tiles not loaded become zeros
-      const int sv = n % SV;
-      uint8_t *vst = smem + L::kVOff + sv * kAtoms * kPairKvAtom;
-      if (lane == 0 && n >= SV && !mbar_wait_bounded(&v_empty[sv], ((n / SV) - 1) & 1))
-        ok_run = false;
-      ok_run = __shfl_sync(kFullMask, ok_run ? 1 : 0, 0) != 0;
-      if (!ok_run) break;
-      __syncwarp();
-      const int key0 = n * kPairKeys;
-      const bool tail = key0 + kPairKeys > n_keys;
-      if (mask != kAllSub) {
-        // sub-tiles with no load: zero every 64-dim atom of their 16 rows
-        for (int i = lane; i < kSub * kAtoms * 16 * 8; i += 32) {  // 16-byte units
-          const int h = i / (kAtoms * 128), b = (i >> 7) % kAtoms, row = (i >> 3) & 15,
-                    u16 = i & 7;
-          if (!((mask >> h) & 1u))
-            *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + (h * 16 + row) * 128 + u16 * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (!tail) {
-        if (lane == 0) {
-          if (bytes == 0)
-            mbar_arrive(&v_full[sv]);
-          else
-            mbar_arrive_expect_tx(&v_full[sv], bytes);
-        }
-        __syncwarp();
-        load(vst, &vmap, &v_full[sv]);
-      } else {
-        // the last step: load, wait, zero the rows past n_keys, then hand over
-        if (lane == 0 && bytes > 0) mbar_arrive_expect_tx(v_tail, bytes);
-        __syncwarp();
-        load(vst, &vmap, v_tail);
-        bool got = true;
-        if (lane == 0 && bytes > 0) got = mbar_wait_bounded(v_tail, 0);
-        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
-        if (!got) {
-          ok_run = false;
-          break;
-        }
-        __syncwarp();
-        const int first = n_keys - key0;  // first row to clear
-        for (int i = lane; i < kPairKeys * kAtoms * 8; i += 32) {
-          const int row = i / (kAtoms * 8), b = (i >> 3) % kAtoms, u16 = i & 7;
-          if (row >= first)
-            *reinterpret_cast<uint4 *>(vst + b * kPairKvAtom + row * 128 + u16 * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&v_full[sv]);
-      }
-    }
     }
     if (!ok_run && lane == 0) atomicOr(a.err, kErrTimeout);
   }
