@@ -196,3 +196,18 @@ def _fp8_status(lib, name, **over):
 ])
 def test_fp8_entry_points_host_validation(lib, name, over, status):
     assert _fp8_status(lib, name, **over) == status
+
+
+def test_binding_matches_cache_type_to_entry_point(lib):
+    """The Python block copies check the cache type before anything reaches
+    the library: the 16-bit form refuses uint8 (FP8) caches, whose blocks are
+    half the bytes, and the FP8 form refuses 16-bit caches."""
+    import torch
+    import pagedattention_kv_cache_attention_gb300 as pa
+    m = torch.zeros(1, 2, dtype=torch.int64)
+    f8 = torch.zeros(4, 2, 16, 64, dtype=torch.uint8)
+    f16 = torch.zeros(4, 2, 16, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="caches must be"):
+        pa.pa_copy_blocks(f8, f8, m)
+    with pytest.raises(ValueError, match="caches must be"):
+        pa.pa_copy_blocks_fp8(f16, f16, m)
