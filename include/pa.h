@@ -26,7 +26,8 @@
  *    stream).  Every compute call only validates its arguments on the host,
  *    enqueues kernels on `stream` and returns; results are ready when the
  *    stream reaches that point.
- *  - Layouts (row-major, element type given by `dtype`, 2 bytes each):
+ *  - Layouts (row-major, element type given by `dtype`, 2 bytes each; the
+ *    caches of the *_fp8 calls hold one-byte codes, see "FP8 KV cache"):
  *      k_cache, v_cache  [num_blocks, num_kv_heads, block_size, head_dim]
  *      query, out        [num_seqs, num_q_heads, head_dim]
  *      block_tables      int32 [num_seqs, max_blocks_per_seq]; entry
@@ -77,7 +78,7 @@ typedef enum pa_dtype {
 #define PA_DEVERR_TIMEOUT   8u   /* a wait for staged KV data ran past its time limit */
 #define PA_DEVERR_WORKSPACE 16u  /* a split-context join counter in the workspace did not
                                     start at zero (see pa_decode_workspace_size) */
-#define PA_DEVERR_PREFIX    32u  /* pa_decode_shared_prefix: the groups do not cover the batch,
+#define PA_DEVERR_PREFIX    32u  /* pa_decode_shared_prefix(_fp8): the groups do not cover the batch,
                                     a group is larger than max_group_size, members of a group
                                     give different prefix lengths, or a member's table names
                                     other blocks than the group's for its shared prefix */
@@ -221,9 +222,8 @@ pa_status pa_decode_reduce(void *out, const void *workspace, const int32_t *cont
  * Other arguments, the workspace (pa_decode_workspace_size bytes, counter
  * words zero) and the accuracy are as for pa_decode; dtype fp16 or bf16
  * caches (FP8 caches: pa_decode_shared_prefix_fp8 below).  Input errors only
- * the device can see set PA_DEVERR_PREFIX (see
- * above): the output of the sequences concerned is then unspecified, never a
- * fault.
+ * the device can see set PA_DEVERR_PREFIX (see above): the output of the
+ * sequences concerned is then unspecified, never a fault.
  */
 pa_status pa_decode_shared_prefix(void *out, const void *query,
                                   const void *k_cache, const void *v_cache,
