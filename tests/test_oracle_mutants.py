@@ -43,6 +43,10 @@ MUTANTS = [
     ("prefill_not_causal_inclusive", "int n = pos + 1;", "int n = pos;"),
     ("prefill_position", "int pos = ctx - q_len + (row - query_start[i]);",
      "int pos = ctx - q_len + (row - query_start[i]) / 2;"),
+    ("prefill_fp8_k_with_v_scale", "rc = pa_oracle_gather(K, k_cache, kv_dtype, k_scale, bt_row, MB, n,",
+     "rc = pa_oracle_gather(K, k_cache, kv_dtype, v_scale, bt_row, MB, n,"),
+    ("prefill_fp8_v_as_query_type", "rc = pa_oracle_gather(V, v_cache, kv_dtype, v_scale, bt_row, MB, n,",
+     "rc = pa_oracle_gather(V, v_cache, dtype, v_scale, bt_row, MB, n,"),
 ]
 
 RUNNER = r"""
